@@ -1,0 +1,118 @@
+"""Seeded synthetic inputs for the attention workloads (no attention math).
+
+This module is the only code shared by the CUDA path's tests/bench and the
+oracle's callers: it draws random tensors and masks and nothing else.
+
+Recipe (the pages name BERT-large seq 512, GPT-2 seq 1K, Long-Range-Arena
+1K-4K, Path-X 16K; these seeded tensors stand in for those workloads):
+  * ``torch.Generator('cpu').manual_seed(seed)``; q, k, v, dO drawn in that
+    order with ``torch.randn(shape, dtype=float32)`` then cast (round to
+    nearest even) to fp16 / bf16;
+  * optional multiplier on q and k after the cast (2 for the long-context
+    sweep; exact, a power of two);
+  * key-padding lengths ``torch.randint(lo, hi + 1, (B,))`` from the same
+    generator, drawn after dO;
+  * block mask ``torch.rand(nb, nb) < p`` from its own generator
+    (``manual_seed(mask_seed)``), diagonal forced to keep.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+BLOCK = 128
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str            # "f16" | "bf16"
+    causal: bool = False
+    kv_len_range: tuple | None = None   # (lo, hi) inclusive
+    block_sparse_p: float | None = None
+    mask_seed: int = 7
+    qk_mult: float = 1.0
+    seed: int = 0
+    backward: bool = True
+    notes: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+
+
+# The five workloads of the method's evaluation, as synthetic stand-ins.
+WORKLOADS = {
+    "fwd_b1_h2_n256_d64_f16": Workload("fwd_b1_h2_n256_d64_f16", 1, 2, 256, 64, "f16",
+                                       backward=False),
+    "bert_b16_h16_n512_d64_f16_kvlen": Workload(
+        "bert_b16_h16_n512_d64_f16_kvlen", 16, 16, 512, 64, "f16", kv_len_range=(256, 512)),
+    "gpt2_b8_h12_n1024_d64_bf16_causal": Workload(
+        "gpt2_b8_h12_n1024_d64_bf16_causal", 8, 12, 1024, 64, "bf16", causal=True),
+    "long_b8_h16_n4096_d128_bf16_causal": Workload(
+        "long_b8_h16_n4096_d128_bf16_causal", 8, 16, 4096, 128, "bf16", causal=True, qk_mult=2.0),
+    "long_b4_h16_n8192_d128_bf16_causal": Workload(
+        "long_b4_h16_n8192_d128_bf16_causal", 4, 16, 8192, 128, "bf16", causal=True, qk_mult=2.0),
+    "long_b2_h16_n16384_d128_bf16_causal": Workload(
+        "long_b2_h16_n16384_d128_bf16_causal", 2, 16, 16384, 128, "bf16", causal=True,
+        qk_mult=2.0),
+    "blocksparse_b2_h8_n16384_d64_f16": Workload(
+        "blocksparse_b2_h8_n16384_d64_f16", 2, 8, 16384, 64, "f16", block_sparse_p=0.2),
+}
+
+
+def make_qkv(B, H, N, d, dtype, seed=0, qk_mult=1.0, with_dout=True,
+             kv_len_range=None):
+    """Draw q, k, v (and dO, kv_len) on the CPU. Returns a dict of tensors."""
+    tdt = torch.float16 if dtype in ("f16", torch.float16) else torch.bfloat16
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
+    k = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
+    v = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
+    out = {"q": q, "k": k, "v": v}
+    if with_dout or kv_len_range is not None:
+        out["dout"] = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
+    if kv_len_range is not None:
+        lo, hi = kv_len_range
+        out["kv_len"] = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(
+            torch.int32)
+    if qk_mult != 1.0:
+        out["q"] = out["q"] * qk_mult
+        out["k"] = out["k"] * qk_mult
+    return out
+
+
+def make_block_mask(N, p, seed=7, block=BLOCK):
+    """uint8 [nb, nb] keep-mask: Bernoulli(p) off the diagonal, diagonal kept."""
+    nb = (N + block - 1) // block
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    m = torch.rand((nb, nb), generator=g) < p
+    m.fill_diagonal_(True)
+    return m.to(torch.uint8)
+
+
+def make_workload(w: Workload, with_dout=None):
+    """All inputs of a named workload (CPU tensors)."""
+    if with_dout is None:
+        with_dout = w.backward
+    t = make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult,
+                 with_dout=with_dout, kv_len_range=w.kv_len_range)
+    if w.block_sparse_p is not None:
+        t["block_mask"] = make_block_mask(w.N, w.block_sparse_p, seed=w.mask_seed)
+    return t
+
+
+def head_slice(t, b, h):
+    """[N, d] view of one head of a [B, H, N, d] tensor."""
+    return t[b, h]
