@@ -1,0 +1,25 @@
+"""Exact IO-aware attention for B300 (sm_103a).
+
+The compute path is the CUDA library ``libfa.so`` (C ABI in include/fa.h);
+this package is its thin Python binding. Importing the package does not
+load the library; the first call does, and fails loudly if it is missing.
+"""
+from ._binding import (  # noqa: F401
+    FAError,
+    FA_F16,
+    FA_BF16,
+    fa_bwd,
+    fa_bwd_blocksparse,
+    fa_bwd_workspace_size,
+    fa_fwd,
+    fa_fwd_blocksparse,
+    fa_fwd_ex,
+    fa_get_device_error,
+    fa_last_error_message,
+    fa_status_str,
+    fa_version,
+    exported_symbols,
+    library_path,
+    load_library,
+)
+from .api import attention_backward, attention_forward  # noqa: F401

@@ -1,0 +1,45 @@
+"""Convenience wrappers: allocate outputs with torch, then call the C ABI."""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _binding as B
+
+
+def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None,
+                      stream=None):
+    """O [B,H,N,d] and LSE [B,H,N] fp32 of exact attention (device tensors)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if block_mask is not None:
+        B.fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, stream=stream)
+    elif kv_len is not None:
+        B.fa_fwd_ex(q, k, v, o, lse, scale, causal, kv_len, stream=stream)
+    else:
+        B.fa_fwd(q, k, v, o, lse, scale, causal, stream=stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=None,
+                       block_mask=None, workspace=None, stream=None):
+    """dQ, dK, dV [B,H,N,d] of exact attention (device tensors)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    Bsz, H, N, d = q.shape
+    ws_bytes = B.fa_bwd_workspace_size(Bsz, H, N, d)
+    if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    if block_mask is not None:
+        B.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, workspace,
+                             stream=stream)
+    else:
+        B.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, kv_len, workspace,
+                 stream=stream)
+    return dq, dk, dv

@@ -1,0 +1,60 @@
+// common.cuh -- device-side helpers shared by the attention kernels:
+// the device error flag and bounded mbarrier waits.
+#pragma once
+#include "ptx.cuh"
+
+namespace fa {
+
+// A pipeline wait that takes longer than this is a bug; the kernel gives up.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+enum : uint32_t { kDevErrTimeout = 1u };
+
+// Device error word, read and cleared by fa_get_device_error(). Kernels and
+// the host code that reads it live in one translation unit (fa_lib.cu).
+__device__ unsigned int g_fa_device_error = 0;
+
+// Slow path of a wait: poll until the phase completes, the CTA-wide abort
+// flag is raised by another role, or the time limit passes (then raise the
+// abort flag and the device error word). honor_abort = false is used when
+// draining copies in flight after an abort.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile uint32_t *abort_flag, bool honor_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 127u) == 0) {
+      if (honor_abort && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicOr(&g_fa_device_error, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait for the phase of `bar` with parity `parity`; false on abort/timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile uint32_t *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, true);
+}
+
+// Same, called by all 32 lanes of a warp; the result is warp-uniform so the
+// warp stays converged for the .sync.aligned tcgen05 instructions after it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile uint32_t *abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                volatile uint32_t *abort_flag) {
+  if (!mbar_try_wait(bar, parity)) mbar_wait_slow(bar, parity, abort_flag, false);
+}
+
+__device__ __forceinline__ uint32_t align_up_1024(uint32_t a) { return (a + 1023u) & ~1023u; }
+
+}  // namespace fa

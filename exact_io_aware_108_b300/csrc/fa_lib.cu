@@ -1,0 +1,276 @@
+// fa_lib.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// checks, TMA tensor-map encoding, kernel dispatch and the device error flag.
+// All device code is included here so the library is one translation unit.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "fa.h"
+#include "fwd_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fa_status fail(fa_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+fa_status ok() {
+  g_last_error.clear();
+  return FA_OK;
+}
+
+fa_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, d] 16-bit tensor viewed as a 3-D TMA map with 64 x 128 x 1 boxes
+// (one 128-byte-wide column block of a 128-row tile), 128-byte swizzle.
+// Rows past N read as zero.
+fa_status make_tile_map(CUtensorMap *m, const void *ptr, fa_dtype dt, int N, long long BH, int d,
+                        const char *name) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, dt == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return FA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Shape {
+  int B, H, N, d;
+  long long BH;
+  int nqt;
+};
+
+fa_status check_common(int B, int H, int N, int d, float scale, fa_dtype dt, Shape *s) {
+  if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d < 1) return fail(FA_ERR_INVALID_ARG, "d must be >= 1 (got %d)", d);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", d);
+  if (dt != FA_F16 && dt != FA_BF16) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  s->B = B;
+  s->H = H;
+  s->N = N;
+  s->d = d;
+  s->BH = static_cast<long long>(B) * H;
+  s->nqt = (N + 127) / 128;
+  if (s->BH * s->nqt > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B*H*ceil(N/128) exceeds 2^31-1");
+  if (s->BH > INT_MAX / 2) return fail(FA_ERR_INVALID_ARG, "B*H too large");
+  return FA_OK;
+}
+
+fa_status check_ptrs(std::initializer_list<std::pair<const void *, const char *>> ps) {
+  for (auto &p : ps) {
+    if (p.first == nullptr) return fail(FA_ERR_INVALID_ARG, "%s is null", p.second);
+    if (!aligned16(p.first)) return fail(FA_ERR_INVALID_ARG, "%s is not 16-byte aligned", p.second);
+  }
+  return FA_OK;
+}
+
+// cudaFuncSetAttribute once per (kernel, device).
+cudaError_t set_smem(const void *kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<const void *, unsigned long long> done;  // kernel -> bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  unsigned long long &bits = done[kernel];
+  if (dev < 64 && ((bits >> dev) & 1ull)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) bits |= 1ull << dev;
+  return e;
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const fa::FwdArgs &a, int grid, cudaStream_t st) {
+  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE>;
+  constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
+  cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+  kern<<<grid, 256, smem, st>>>(tq, tk, tv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
+  return FA_OK;
+}
+
+template <int D, bool BF16>
+fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
+  if (sparse) return launch_fwd_t<D, BF16, false, true>(tq, tk, tv, a, grid, st);
+  if (causal) return launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st);
+  return launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
+}
+
+fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, fa_dtype dt, const int32_t *kv_len,
+                   const uint8_t *block_mask, bool sparse, void *stream) {
+  Shape s;
+  fa_status r = check_common(B, H, N, d, scale, dt, &s);
+  if (r != FA_OK) return r;
+  r = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
+  if (r != FA_OK) return r;
+  if (sparse) {
+    if (block_mask == nullptr) return fail(FA_ERR_INVALID_ARG, "block_mask is null");
+    if (s.nqt > fa::FwdCfg<64>::kMaxList)
+      return fail(FA_ERR_UNSUPPORTED, "block-sparse needs ceil(N/128) <= %d", fa::FwdCfg<64>::kMaxList);
+  }
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "kv_len is not 4-byte aligned");
+  CUtensorMap tq, tk, tv;
+  if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
+  if ((r = make_tile_map(&tk, k, dt, N, s.BH, d, "k")) != FA_OK) return r;
+  if ((r = make_tile_map(&tv, v, dt, N, s.BH, d, "v")) != FA_OK) return r;
+  fa::FwdArgs a;
+  a.o = o;
+  a.lse = lse;
+  a.kv_len = kv_len;
+  a.block_mask = block_mask;
+  a.H = H;
+  a.N = N;
+  a.nqt = s.nqt;
+  a.nkt = s.nqt;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = static_cast<int>(s.BH * s.nqt);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool c = causal != 0;
+  if (d == 64)
+    r = dt == FA_BF16 ? launch_fwd_d<64, true>(tq, tk, tv, a, grid, c, sparse, st)
+                      : launch_fwd_d<64, false>(tq, tk, tv, a, grid, c, sparse, st);
+  else
+    r = dt == FA_BF16 ? launch_fwd_d<128, true>(tq, tk, tv, a, grid, c, sparse, st)
+                      : launch_fwd_d<128, false>(tq, tk, tv, a, grid, c, sparse, st);
+  if (r != FA_OK) return r;
+  return ok();
+}
+
+size_t fa_bwd_ws_bytes(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return up(rows * 4) + up(rows * static_cast<size_t>(d) * 4);
+}
+
+fa_status bwd_impl(const void *, const void *, const void *, const void *, const float *,
+                   const void *, void *, void *, void *, int, int, int, int, float, int, fa_dtype,
+                   const int32_t *, const uint8_t *, bool, void *, size_t, void *) {
+  return fail(FA_ERR_UNSUPPORTED, "backward not built yet");
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int N, int d, float scale, int causal, fa_dtype dtype, void *stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nullptr, nullptr, false,
+                  stream);
+}
+
+fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                    int N, int d, float scale, int causal, fa_dtype dtype, const int32_t *kv_len,
+                    void *stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
+                  stream);
+}
+
+fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, fa_dtype dtype,
+                             const uint8_t *block_mask, void *stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, 0, dtype, nullptr, block_mask, true, stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  return fa_bwd_ws_bytes(B, H, N, d);
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, const int32_t *kv_len, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, dtype, kv_len,
+                  nullptr, false, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int B, int H, int N, int d, float scale, fa_dtype dtype,
+                             const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, 0, dtype, nullptr,
+                  block_mask, true, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_get_device_error(void *stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, fa::g_fa_device_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error flag");
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(fa::g_fa_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error flag");
+    return fail(FA_ERR_TIMEOUT, "a kernel pipeline wait timed out (flag 0x%x)", v);
+  }
+  return ok();
+}
+
+const char *fa_status_str(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+const char *fa_last_error_message(void) { return g_last_error.c_str(); }
+
+const char *fa_version(void) { return "0.1.0"; }
+
+}  // extern "C"

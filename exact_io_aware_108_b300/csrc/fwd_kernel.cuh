@@ -1,0 +1,376 @@
+// fwd_kernel.cuh -- forward attention kernel for sm_103a.
+//
+// One CTA computes one 128-row query tile of one (batch, head): the block
+// loop of "Flash Attention: revolutionizing transformer efficiency" (sections
+// "The Flash Attention Algorithm" and "Implementation Details": query block
+// outer, key/value blocks inner, running row max m and row sum l), with the
+// output kept unnormalised in TMEM and divided by l once at the end.
+//
+// Roles (256 threads):
+//   warp 0, lane 0  TMA producer: Q tile once, then K_j / V_j tiles through a
+//                   ring of shared-memory stages (128-byte swizzle).
+//   warp 1          allocates TMEM; lane 0 issues every tcgen05.mma:
+//                   S_j = Q K_j^T into one of two TMEM score buffers, and
+//                   O += P_j V_j with P_j read from TMEM.
+//   warp 2          builds the kept-tile list of a block-sparse row.
+//   warps 4..7      softmax: thread r owns query row r (TMEM lane r). Reads
+//                   S_j, applies the mask, updates m and l, writes P_j as
+//                   16-bit values to TMEM, rescales the O row when m grows,
+//                   and finally writes O / l and LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 and P1 (64
+// columns each, two 16-bit probabilities per column) after O.
+//
+// Online softmax in base 2: x = s * scale * log2(e); p = 2^(x - m);
+// l <- 2^(m_old - m) l + sum p; O <- 2^(m_old - m) O + P V
+// (softmax decomposition and merger, section "The Math Behind Flash
+// Attention"). m is only moved when the row max grows by more than 8 (a
+// factor 256), so most tiles need no O rescale; O, l and the final LSE all
+// use the same m, so the result is unchanged.
+#pragma once
+#include "common.cuh"
+
+namespace fa {
+
+struct FwdArgs {
+  void *o;
+  float *lse;
+  const int32_t *kv_len;     // [B] or null
+  const uint8_t *block_mask; // [nkt, nkt] or null
+  int H, N, nqt, nkt;
+  float scale_log2;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile, 16-bit
+  static constexpr int kStages = (D == 64) ? 4 : 2; // K/V ring depth
+  static constexpr int kKB = D / 64;                // 128-byte column blocks
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O ready, drain
+  static constexpr int kBQ = 0;
+  static constexpr int kBKF = 1;
+  static constexpr int kBVF = kBKF + kStages;
+  static constexpr int kBKE = kBVF + kStages;
+  static constexpr int kBVE = kBKE + kStages;
+  static constexpr int kBSF = kBVE + kStages;
+  static constexpr int kBPF = kBSF + 2;
+  static constexpr int kBOR = kBPF + 2;
+  static constexpr int kBDR = kBOR + 1;
+  static constexpr int kNumBars = kBDR + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, list count
+  static constexpr int kListOff = kMiscOff + 16;
+  static constexpr int kMaxList = 2048;                     // block-sparse: nkt <= 2048
+  static constexpr int kSmemBytes = kListOff + kMaxList * 2 + 1024;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kColP0 = 256 + D, kColP1 = 256 + D + 64;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColP1 + 64 <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+__global__ void __launch_bounds__(256, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = align_up_1024(raw);
+  uint8_t *smem = smem_raw + (sbase - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  volatile uint32_t *abort_flag = misc + 1;
+  uint16_t *list = reinterpret_cast<uint16_t *>(smem + C::kListOff);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
+
+  // ---- work item: heads are contiguous in the grid so concurrent CTAs share
+  // K/V in L2; causal rows run heaviest tile first.
+  const int bh = blockIdx.x / a.nqt;
+  int qt = blockIdx.x % a.nqt;
+  if (CAUSAL) qt = a.nqt - 1 - qt;
+  const int b = bh / a.H;
+  int kvl = a.N;
+  if (a.kv_len != nullptr) {
+    const int v = a.kv_len[b];
+    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
+  }
+  const int nkt_eff = (kvl + 127) >> 7;
+
+  if (tid == 0) {
+    mbar_init(bar(C::kBQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBKF + s), 1);
+      mbar_init(bar(C::kBVF + s), 1);
+      mbar_init(bar(C::kBKE + s), 1);
+      mbar_init(bar(C::kBVE + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kBSF + s), 1);
+      mbar_init(bar(C::kBPF + s), 128);
+    }
+    mbar_init(bar(C::kBOR), 1);
+    mbar_init(bar(C::kBDR), 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (SPARSE && warp == 2) {
+    // kept key tiles of this query tile, in increasing order
+    const uint8_t *mrow = a.block_mask + static_cast<size_t>(qt) * a.nkt;
+    int cnt = 0;
+    for (int j0 = 0; j0 < nkt_eff; j0 += 32) {
+      const int j = j0 + lane;
+      const bool keep = (j < nkt_eff) && (mrow[j] != 0);
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) list[cnt + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(j);
+      cnt += __popc(bal);
+    }
+    if (lane == 0) misc[2] = static_cast<uint32_t>(cnt);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int n_tiles = SPARSE ? static_cast<int>(misc[2])
+                             : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_tiles > 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes);
+      for (int kb = 0; kb < C::kKB; ++kb)
+        tma_load_3d_hint(sbase + C::kQOff + kb * 16384, &tm_q, bar(C::kBQ), kb * 64, qt * 128, bh,
+                         pol_q);
+      int nk = 0, nv = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % C::kStages;
+        const uint32_t ph = (t / C::kStages) & 1;
+        const int kt = SPARSE ? list[t] : t;
+        if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
+                           bar(C::kBKF + st), kb * 64, kt * 128, bh, pol_kv);
+        nk = t + 1;
+        if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
+                           bar(C::kBVF + st), kb * 64, kt * 128, bh, pol_kv);
+        nv = t + 1;
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the CTA exits
+        mbar_wait_drain(bar(C::kBQ), 0, abort_flag);
+        for (int t = max(0, nk - C::kStages); t < nk; ++t)
+          mbar_wait_drain(bar(C::kBKF + t % C::kStages), (t / C::kStages) & 1, abort_flag);
+        for (int t = max(0, nv - C::kStages); t < nv; ++t)
+          mbar_wait_drain(bar(C::kBVF + t % C::kStages), (t / C::kStages) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_f16(BF16, 128, D, false, true);
+      bool ok = mbar_wait(bar(C::kBQ), 0, abort_flag);
+      tc_fence_after();
+      auto issue_pv = [&](int u) -> bool {
+        const int st = u % C::kStages;
+        const uint32_t ph = (u / C::kStages) & 1;
+        const int pb = u & 1;
+        if (!mbar_wait(bar(C::kBPF + pb), (u >> 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
+        const uint32_t pcol = tmem + (pb ? C::kColP1 : C::kColP0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
+          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
+          mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBVE + st));
+        mma_commit(bar(C::kBOR));
+        return true;
+      };
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % C::kStages;
+        const uint32_t ph = (t / C::kStages) & 1;
+        const int sb = t & 1;
+        if (!mbar_wait(bar(C::kBKF + st), ph, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
+        const uint32_t scol = tmem + (sb ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          // A = Q, B = K_j, both K-major: 16 head-dim elements = 32 B per step
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
+                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBSF + sb));
+        mma_commit(bar(C::kBKE + st));
+        if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(n_tiles - 1);
+      // every issued MMA must finish before TMEM is released
+      mma_commit(bar(C::kBDR));
+      mbar_wait_drain(bar(C::kBDR), 0, abort_flag);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int row = tid - 128;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int q_row = qt * 128 + row;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int sb = t & 1;
+      const int kt = SPARSE ? list[t] : t;
+      if (!mbar_wait_warp(bar(C::kBSF + sb), (t >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        const uint32_t scol = tmem + lane_addr + (sb ? C::kColS1 : C::kColS0);
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld_32x32b_x32(scol + 0, r0);
+        tmem_ld_32x32b_x32(scol + 32, r1);
+        tmem_ld_32x32b_x32(scol + 64, r2);
+        tmem_ld_32x32b_x32(scol + 96, r3);
+        tmem_wait_ld();
+        reg_fence_32(r0);
+        reg_fence_32(r1);
+        reg_fence_32(r2);
+        reg_fence_32(r3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(r0[c]);
+          s[32 + c] = __uint_as_float(r1[c]);
+          s[64 + c] = __uint_as_float(r2[c]);
+          s[96 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      // mask: keys past kv_len / N, and keys after the query on the diagonal
+      int limit = kvl - kt * 128;
+      if (CAUSAL && kt == qt) limit = min(limit, row + 1);
+      if (limit < 128) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= limit) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = (mxs > m + 8.0f) ? mxs : m;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
+        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
+        s[c + 2] = ex2_approx(fmaf(s[c + 2], sl2, -m_use));
+        s[c + 3] = ex2_approx(fmaf(s[c + 3], sl2, -m_use));
+        rs0 += s[c];
+        rs1 += s[c + 1];
+        rs2 += s[c + 2];
+        rs3 += s[c + 3];
+      }
+      l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
+      if (t > 0) {
+        // O holds P_{t-1} V_{t-1} only once that MMA is done
+        if (!mbar_wait_warp(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, m_new != m)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c0, o);
+            tmem_wait_ld();
+            reg_fence_32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_32x32b_x32(tmem + lane_addr + C::kColO + c0, o);
+          }
+        }
+      }
+      {
+        const uint32_t pcol = tmem + lane_addr + (sb ? C::kColP1 : C::kColP0);
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
+          tmem_st_32x32b_x16(pcol + c0 / 2, pk);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBPF + sb));
+      m = m_new;
+    }
+    // ---- epilogue: O / l and LSE
+    bool have_o = ok && n_tiles > 0;
+    if (have_o) {
+      have_o = mbar_wait_warp(bar(C::kBOR), (n_tiles - 1) & 1, abort_flag);
+      tc_fence_after();
+    }
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    uint16_t *orow = static_cast<uint16_t *>(a.o) +
+                     (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c0, o);
+        tmem_wait_ld();
+        reg_fence_32(o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (q_row < a.N) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+    if (q_row < a.N)
+      a.lse[static_cast<size_t>(bh) * a.N + q_row] =
+          (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

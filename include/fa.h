@@ -1,0 +1,160 @@
+/*
+ * fa.h -- C ABI of the exact IO-aware attention library (libfa.so).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T + M) V
+ *
+ * ("Flash Attention: revolutionizing transformer efficiency", standard
+ * attention listing, and the FlashAttention abstract on the Tri Dao author
+ * page: "an IO-aware exact attention algorithm that uses tiling"), tile by
+ * tile on the GPU with the online-softmax rescaling of the same page (section
+ * "The Math Behind Flash Attention": softmax decomposition and merger), so the
+ * N x N score matrix never reaches device memory. The forward pass also writes
+ * the per-row log-sum-exp; the backward pass recomputes the score tiles from
+ * Q, K and that log-sum-exp (same page, key idea 2, "Recomputation").
+ *
+ * M is 0 where a key is visible and -inf where it is masked:
+ *   causal       key j is masked for query i when j > i (top-left aligned);
+ *   key padding  key j is masked for every query of batch b when
+ *                j >= kv_len[b];
+ *   block-sparse the 128 x 128 tile (i / 128, j / 128) is skipped entirely
+ *                when block_mask[(i / 128) * nb + j / 128] == 0
+ *                (block-sparse FlashAttention, same abstract).
+ * A query row with no visible key gets O = 0 and LSE = -inf and contributes
+ * nothing to any gradient.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout    q, k, v, o, dout, dq, dk, dv are contiguous [B, H, N, d] arrays of
+ *           16-bit floats (fp16 or bf16, chosen by `dtype`), d fastest; lse is
+ *           a contiguous fp32 [B, H, N] array holding the NATURAL-log
+ *           log-sum-exp of the scaled, masked scores of each row. Queries and
+ *           keys have the same length N (self-attention).
+ * Sizes     B >= 1, H >= 1, N >= 1, d in {64, 128}; B * H <= 65535 * 65535.
+ * Memory    every pointer is a DEVICE pointer owned by the caller, 16-byte
+ *           aligned, on the current CUDA device. The library allocates no
+ *           device memory; the backward takes a caller-owned workspace.
+ *           Outputs must not alias inputs.
+ * Streams   `stream` is a cudaStream_t (NULL = legacy default stream). Every
+ *           call is asynchronous on that stream and never synchronises, except
+ *           fa_get_device_error.
+ * Numerics  inputs are read as fp16/bf16; every product is accumulated in fp32;
+ *           the softmax runs in fp32 with exp2; probabilities are rounded to
+ *           the input type before the P V product.
+ * Errors    argument checks run on the host before any launch and return
+ *           FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED without touching memory.
+ *           A failed launch returns FA_ERR_CUDA. A pipeline wait inside a
+ *           kernel that exceeds its time limit (about two seconds; it cannot
+ *           happen in a correct build) makes the kernel stop early and sets a
+ *           device flag that fa_get_device_error reports as FA_ERR_TIMEOUT.
+ *           fa_last_error_message() gives the detail of the last failure on
+ *           the calling thread.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer   */
+    FA_ERR_UNSUPPORTED = 2,  /* valid but not built: d not in {64, 128}     */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed           */
+    FA_ERR_TIMEOUT = 4       /* a kernel pipeline wait ran out (device flag) */
+} fa_status;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+#define FA_BLOCK 128 /* tile edge: rows of a query tile and keys of a key tile */
+
+/*
+ * Forward pass: O and LSE of exact attention, dense (causal = 0) or causal
+ * (causal != 0). The block loop with running row max m and row sum l
+ * ("Flash Attention: revolutionizing transformer efficiency", sections "The
+ * Flash Attention Algorithm" and "Implementation Details"; corrected so the
+ * output is normalised once, at the end).
+ *   q, k, v  [B,H,N,d] in;   o [B,H,N,d] out;   lse [B,H,N] fp32 out.
+ *   scale    multiplier of Q K^T (1/sqrt(d) for standard attention).
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 fa_dtype dtype, void *stream);
+
+/*
+ * fa_fwd with key padding: kv_len is a DEVICE int32 [B] array (or NULL for
+ * none); keys j >= kv_len[b] are masked for all queries of batch b. Values
+ * above N act as N; values below 1 mask every key of that batch.
+ */
+fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    fa_dtype dtype, const int32_t *kv_len, void *stream);
+
+/*
+ * Block-sparse forward (FlashAttention abstract: "We also extend
+ * FlashAttention to block-sparse attention"). block_mask is a DEVICE uint8
+ * array [nb, nb], nb = ceil(N / 128), row = query tile, column = key tile,
+ * nonzero = keep, shared by all (b, h). Masked tiles are neither loaded nor
+ * multiplied; inside a kept tile attention is dense and non-causal.
+ */
+fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o,
+                             float *lse, int B, int H, int N, int d, float scale,
+                             fa_dtype dtype, const uint8_t *block_mask, void *stream);
+
+/*
+ * Bytes of device workspace fa_bwd / fa_bwd_blocksparse need for these
+ * sizes: fp32 D = rowsum(dO * O) [B,H,N] and an fp32 dQ accumulator
+ * [B,H,N,d], each rounded up to 256 bytes. Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass. The gradient of O = softmax(scale Q K^T + M) V with respect
+ * to Q, K, V given dO, recomputing P tile by tile from Q, K and LSE instead of
+ * storing it (key idea 2 of "Flash Attention: revolutionizing transformer
+ * efficiency"):
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, o, dout [B,H,N,d] in; lse [B,H,N] in (from the forward with the
+ *   same arguments); dq, dk, dv [B,H,N,d] out; kv_len as in fa_fwd_ex.
+ *   workspace: DEVICE memory of at least fa_bwd_workspace_size(B,H,N,d)
+ *   bytes, 256-byte aligned, owned by the caller, contents ignored on entry.
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                 int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                 const int32_t *kv_len, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/* Block-sparse backward: fa_bwd with the block mask of fa_fwd_blocksparse. */
+fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk,
+                             void *dv, int B, int H, int N, int d, float scale,
+                             fa_dtype dtype, const uint8_t *block_mask, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error flag set by
+ * a kernel whose pipeline wait timed out. Returns FA_OK, FA_ERR_TIMEOUT or
+ * FA_ERR_CUDA (when the synchronisation itself failed).
+ */
+fa_status fa_get_device_error(void *stream);
+
+/* Static string naming a status code. */
+const char *fa_status_str(fa_status status);
+
+/* Detail of the last failed call on this host thread ("" if none). */
+const char *fa_last_error_message(void);
+
+/* Library version string ("major.minor.patch"). */
+const char *fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H_ */

@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/fa.h declares, and rejects bad arguments before any
+launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_108_b300 as fa
+from exact_io_aware_108_b300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fa.load_library()
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    missing = [n for n in declared if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(_binding.EXPORTS) == declared
+
+
+def test_status_strings_and_version():
+    assert fa.fa_status_str(0) == "FA_OK"
+    assert fa.fa_status_str(4) == "FA_ERR_TIMEOUT"
+    assert re.match(r"^\d+\.\d+\.\d+$", fa.fa_version())
+
+
+def test_workspace_size():
+    def up(x):
+        return (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == up(2 * 3 * 300 * 4) + up(2 * 3 * 300 * 64 * 4)
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address that is never dereferenced
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+         causal=0, dt=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), causal, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"q": None}, 1), ({"o": None}, 1), ({"lse": None}, 1),
+    ({"k": FAKE + 8}, 1),
+    ({"B": 0}, 1), ({"N": 0}, 1), ({"H": -1}, 1), ({"d": 0}, 1),
+    ({"d": 96}, 2), ({"d": 256}, 2),
+    ({"scale": 0.0}, 1), ({"scale": float("nan")}, 1), ({"scale": -1.0}, 1),
+    ({"dt": 7}, 1),
+    ({"B": 70000, "H": 70000, "N": 1 << 20}, 1),
+])
+def test_fwd_rejects_bad_arguments(kw, status):
+    lib = fa.load_library()
+    assert _fwd(lib, **kw) == status
+    assert fa.fa_last_error_message() != ""
+
+
+def test_bwd_rejects_bad_arguments():
+    lib = fa.load_library()
+    c = ctypes.c_float(0.125)
+    args = [FAKE] * 9
+    # workspace too small
+    st = lib.fa_bwd(*args, 1, 1, 128, 64, c, 0, 0, None, FAKE, 16, None)
+    assert st == 1
+    # null dq
+    a2 = list(args)
+    a2[6] = None
+    st = lib.fa_bwd(*a2, 1, 1, 128, 64, c, 0, 0, None, FAKE, 1 << 30, None)
+    assert st == 1
+    # block-sparse without a mask
+    st = lib.fa_bwd_blocksparse(*args, 1, 1, 128, 64, c, 0, None, FAKE, 1 << 30, None)
+    assert st == 1
+
+
+def test_blocksparse_rejects_missing_mask():
+    lib = fa.load_library()
+    st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
+                                None, None)
+    assert st == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.load_library()
