@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention (forward + backward) on B300.
+
+One step = forward and backward of every point of the long-context causal
+sequence sweep (N = 4096, 8192, 16384; B * N = 32768; H = 16; d = 128; bf16;
+Q and K scaled by 2), through the library's C ABI. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs the same per-rank workload on its own
+GPU (independent problems, no collective on the data path; weak scaling);
+the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s and % of B300 fp16/bf16 tensor peak vs seq len"
+SWEEP = [
+    "long_b8_h16_n4096_d128_bf16_causal",
+    "long_b4_h16_n8192_d128_bf16_causal",
+    "long_b2_h16_n16384_d128_bf16_causal",
+]
+WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, B*N = 32768, "
+                 "H = 16, d = 128, bf16, Q and K scaled by 2; one step = fwd + bwd of all three")
+
+# DRAM traffic of one bwd_main_kernel launch per sweep point, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# sources hashed in "source_sha256"; see profiles/.
+TRAFFIC = {"source_sha256": None, "bytes_per_launch": {}}
+KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
+                  "exact_io_aware_108_b300/csrc/common.cuh",
+                  "exact_io_aware_108_b300/csrc/ptx.cuh"]
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def flops_fwd(w, density=1.0):
+    return 4.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0) * density
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw," +
+             ",".join("clocks_event_reasons." + r for r in REASONS))
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 3 + len(REASONS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for r, v in zip(REASONS, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(r)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Problem:
+    """Device buffers of one sweep point; step() = fwd + bwd through the C ABI."""
+
+    def __init__(self, w, seed_offset, device):
+        import torch
+        from exact_io_aware_108_b300 import inputs
+        import exact_io_aware_108_b300 as fa
+        self.w = w
+        self.fa = fa
+        host = inputs.make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed + seed_offset,
+                               qk_mult=w.qk_mult, with_dout=True)
+        self.host = {n: host[n].pin_memory() for n in ("q", "k", "v", "dout")}
+        self.dev = {n: t.to(device) for n, t in self.host.items()}
+        q = self.dev["q"]
+        self.o = torch.empty_like(q)
+        self.o_res = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
+        self.dq = torch.empty_like(q)
+        self.dk = torch.empty_like(q)
+        self.dv = torch.empty_like(q)
+        self.ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                              device=device)
+        self.out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                         for n, t in (("o", self.o), ("lse", self.lse), ("dq", self.dq),
+                                      ("dk", self.dk), ("dv", self.dv))}
+        self.flops_fwd = flops_fwd(w)
+        self.flops_bwd = 2.5 * self.flops_fwd
+
+    def step(self, stream, main_events=None, fwd_events=None):
+        fa, w, d = self.fa, self.w, self.dev
+        if fwd_events is not None:
+            fwd_events[0].record(stream)
+        fa.fa_fwd_ex(d["q"], d["k"], d["v"], self.o, self.lse, w.scale, w.causal, None,
+                     o_res=self.o_res, stream=stream)
+        if fwd_events is not None:
+            fwd_events[1].record(stream)
+        fa.fa_bwd_prepare(self.o, self.o_res, self.lse, d["dout"], self.ws, stream=stream)
+        if main_events is not None:
+            main_events[0].record(stream)
+        fa.fa_bwd_main(d["q"], d["k"], d["v"], d["dout"], self.dk, self.dv, w.scale, w.causal,
+                       workspace=self.ws, stream=stream)
+        if main_events is not None:
+            main_events[1].record(stream)
+        fa.fa_bwd_finish(self.dq, self.ws, stream=stream)
+
+    def step_e2e(self, stream):
+        """Host buffers in, host buffers out, through the public API."""
+        for n in ("q", "k", "v", "dout"):
+            self.dev[n].copy_(self.host[n], non_blocking=True)
+        self.step(stream)
+        for n, t in (("o", self.o), ("lse", self.lse), ("dq", self.dq), ("dk", self.dk),
+                     ("dv", self.dv)):
+            self.out_host[n].copy_(t, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.out_host.values())
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import exact_io_aware_108_b300 as fa
+    from exact_io_aware_108_b300 import inputs
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    fa.load_library()
+    peaks = load_peaks()
+    probs = [Problem(inputs.WORKLOADS[n], rank, device) for n in SWEEP]
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for p in probs:
+                p.step(stream)
+    barrier()
+    assert fa.fa_get_device_error(stream) == 0, "device error during warm-up"
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_uuid = None
+    K = args.steps
+    main_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in probs] for _ in range(K)]
+    fwd_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in probs] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(gpu_uuid) as clocks:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for s in range(K):
+                for i, p in enumerate(probs):
+                    p.step(stream, main_events=main_ev[s][i], fwd_events=fwd_ev[s][i])
+            t1.record(stream)
+        barrier()
+    ms_total = t0.elapsed_time(t1)
+    assert fa.fa_get_device_error(stream) == 0, "device error in the timed region"
+    ms_max = ms_total
+    if dist is not None:
+        tt = torch.tensor([ms_total], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    ms_step = ms_max / K
+    flops_step = sum(p.flops_fwd + p.flops_bwd for p in probs)
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # per-sweep-point breakdown and the dominant kernel (bwd_main) roofline
+    sweep = []
+    main_ms_total = 0.0
+    main_flops_total = 0.0
+    for i, p in enumerate(probs):
+        f_ms = sum(fwd_ev[s][i][0].elapsed_time(fwd_ev[s][i][1]) for s in range(K)) / K
+        m_ms = sum(main_ev[s][i][0].elapsed_time(main_ev[s][i][1]) for s in range(K)) / K
+        main_ms_total += m_ms
+        main_flops_total += p.flops_bwd
+        sweep.append({
+            "N": p.w.N, "B": p.w.B,
+            "fwd_ms": round(f_ms, 4),
+            "fwd_tflops": round(p.flops_fwd / (f_ms * 1e-3) / 1e12, 1),
+            "fwd_frac_of_measured_burst": round(p.flops_fwd / (f_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "bwd_main_ms": round(m_ms, 4),
+            "bwd_main_tflops": round(p.flops_bwd / (m_ms * 1e-3) / 1e12, 1),
+            "bwd_main_frac_of_measured_burst": round(p.flops_bwd / (m_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+        })
+    achieved = main_flops_total / (main_ms_total * 1e-3) / 1e12
+    traffic = None
+    if TRAFFIC["source_sha256"] == kernel_sha() and TRAFFIC["bytes_per_launch"]:
+        vals = [TRAFFIC["bytes_per_launch"].get(str(p.w.N)) for p in probs]
+        if all(v is not None for v in vals):
+            traffic = sum(vals) / len(vals)
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "bwd_main_kernel<d=128,bf16,causal> (3 launches per step)",
+                "peak_kind": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+                "frac_of_measured_burst": round(achieved / peaks["bf16_tflops"], 4)}
+
+    # end to end: pinned host inputs -> device -> fwd+bwd -> host outputs
+    e2e_k = max(1, K // 2)
+    with torch.cuda.stream(stream):
+        p0 = probs[0]
+        for p in probs:
+            p.step_e2e(stream)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_k):
+            for p in probs:
+                p.step_e2e(stream)
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_k
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": sum(p.h2d_bytes() for p in probs),
+           "d2h_bytes_per_step": sum(p.d2h_bytes() for p in probs),
+           "ms_per_step": round(e2e_ms, 3)}
+    del p0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), Q and K x2)",
+        "config": {
+            "workload": WORKLOAD_NAME, "H": 16, "d": 128, "causal": True,
+            "flops_per_step_per_gpu": flops_step,
+            "flop_count": "fwd 4*B*H*N^2*d/2 (causal), bwd 2.5x fwd",
+            "l2": "no flush: every input tensor (134 MB) is larger than the 126 MB L2",
+            "frac_of_measured_burst": round(value / world / peaks["bf16_tflops"], 4),
+            "frac_of_measured_sustained": round(value / world / peaks["bf16_tflops_sustained"], 4),
+            "sweep": sweep, "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * len(probs) * 4,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU (oracle)
+
+def _oracle_head_inputs(n_heads):
+    """The first n_heads heads (b = 0) of the N = 4096 sweep point, on the CPU."""
+    from exact_io_aware_108_b300 import inputs
+    w = inputs.WORKLOADS[SWEEP[0]]
+    t = inputs.make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult)
+    sl = slice(0, n_heads)
+    return w, {n: t[n][0:1, sl].contiguous() for n in ("q", "k", "v", "dout")}
+
+
+def _oracle_step(w, t, nthreads):
+    from oracle import ref
+    ref.attn_fwd(t["q"], t["k"], t["v"], w.scale, w.causal, nthreads=nthreads)
+    ref.attn_bwd(t["q"], t["k"], t["v"], t["dout"], w.scale, w.causal, rows_per_task=256,
+                 nthreads=nthreads)
+
+
+def cpu_baseline(args, n_heads=16):
+    """The fp64 oracle, as it stands, on this host's cores: fwd + bwd of
+    n_heads full heads (all 4096 rows each) of the N = 4096 sweep point."""
+    from oracle import ref
+    ref.load()
+    nthreads = os.cpu_count() or 1
+    w, t = _oracle_head_inputs(n_heads)
+    t0 = time.perf_counter()
+    _oracle_step(w, t, nthreads)
+    sec = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * n_heads * w.N * w.N * w.d * 0.5
+    return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"fwd+bwd of {n_heads} heads (b=0, h=0..{n_heads - 1}) of the N=4096 point, "
+                      f"all rows, fp64; {sec:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: every step is fwd + bwd of one full head
+    of the N = 4096 sweep point on the host cores."""
+    if rank != 0:
+        return
+    from oracle import ref
+    ref.load()
+    nthreads = os.cpu_count() or 1
+    w, t = _oracle_head_inputs(1)
+    for _ in range(args.warmup):
+        _oracle_step(w, t, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, t, nthreads)
+    sec = (time.perf_counter() - t0) / args.steps
+    flops = 3.5 * 4.0 * w.N * w.N * w.d * 0.5
+    value = round(flops / sec / 1e12, 6)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), Q and K x2)",
+        "config": {"workload": WORKLOAD_NAME,
+                   "sample_per_step": "fwd+bwd of one full head (b=0, h=0) of the N=4096 point"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                         "sample": "fwd+bwd of one full head of the N=4096 point per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

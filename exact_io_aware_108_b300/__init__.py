@@ -10,6 +10,9 @@ from ._binding import (  # noqa: F401
     FA_BF16,
     fa_bwd,
     fa_bwd_blocksparse,
+    fa_bwd_finish,
+    fa_bwd_main,
+    fa_bwd_prepare,
     fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_blocksparse,

@@ -19,8 +19,8 @@ FA_F16, FA_BF16 = 0, 1
 # every symbol include/fa.h declares
 EXPORTS = (
     "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_bwd_workspace_size", "fa_bwd",
-    "fa_bwd_blocksparse", "fa_get_device_error", "fa_status_str", "fa_last_error_message",
-    "fa_version",
+    "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish",
+    "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
 )
 
 _lock = threading.Lock()
@@ -58,13 +58,17 @@ def load_library():
         lib = ctypes.CDLL(LIB_PATH)
         fwd = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i]
         lib.fa_fwd.argtypes = fwd + [_vp]
-        lib.fa_fwd_ex.argtypes = fwd + [_vp, _vp]
-        lib.fa_fwd_blocksparse.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]
+        lib.fa_fwd_ex.argtypes = fwd + [_vp, _vp, _vp]
+        lib.fa_fwd_blocksparse.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp,
+                                           _vp]
         lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_bwd_workspace_size.restype = _sz
         bwd = [_vp] * 9 + [_i, _i, _i, _i, _f]
-        lib.fa_bwd.argtypes = bwd + [_i, _i, _vp, _vp, _sz, _vp]
-        lib.fa_bwd_blocksparse.argtypes = bwd + [_i, _vp, _vp, _sz, _vp]
+        lib.fa_bwd.argtypes = bwd + [_i, _i, _vp, _vp, _vp, _sz, _vp]
+        lib.fa_bwd_blocksparse.argtypes = bwd + [_i, _vp, _vp, _vp, _sz, _vp]
+        lib.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_main.argtypes = [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
+        lib.fa_bwd_finish.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_get_device_error.argtypes = [_vp]
         lib.fa_status_str.argtypes = [_i]
         lib.fa_status_str.restype = ctypes.c_char_p
@@ -73,7 +77,7 @@ def load_library():
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_blocksparse",
-                     "fa_get_device_error"):
+                     "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
             getattr(lib, name).restype = _i
         _lib = lib
         return lib
@@ -129,19 +133,19 @@ def fa_fwd(q, k, v, o, lse, scale, causal=False, stream=None):
            "fa_fwd")
 
 
-def fa_fwd_ex(q, k, v, o, lse, scale, causal=False, kv_len=None, stream=None):
+def fa_fwd_ex(q, k, v, o, lse, scale, causal=False, kv_len=None, o_res=None, stream=None):
     B, H, N, d = _dims(q)
     _check(load_library().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                                     float(scale), int(bool(causal)), _dtype_code(q), _ptr(kv_len),
-                                    _stream(stream)),
+                                    _ptr(o_res), _stream(stream)),
            "fa_fwd_ex")
 
 
-def fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, stream=None):
+def fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, o_res=None, stream=None):
     B, H, N, d = _dims(q)
     _check(load_library().fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                              N, d, float(scale), _dtype_code(q), _ptr(block_mask),
-                                             _stream(stream)),
+                                             _ptr(o_res), _stream(stream)),
            "fa_fwd_blocksparse")
 
 
@@ -149,29 +153,60 @@ def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
 
-def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal=False, kv_len=None, workspace=None,
-           workspace_bytes=None, stream=None):
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal=False, kv_len=None, o_res=None,
+           workspace=None, workspace_bytes=None, stream=None):
     B, H, N, d = _dims(q)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                  _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                 int(bool(causal)), _dtype_code(q), _ptr(kv_len), _ptr(workspace),
-                                 int(workspace_bytes), _stream(stream)),
+                                 int(bool(causal)), _dtype_code(q), _ptr(kv_len), _ptr(o_res),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "fa_bwd")
 
 
-def fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, workspace=None,
-                       workspace_bytes=None, stream=None):
+def fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, o_res=None,
+                       workspace=None, workspace_bytes=None, stream=None):
     B, H, N, d = _dims(q)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load_library().fa_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
                                              float(scale), _dtype_code(q), _ptr(block_mask),
-                                             _ptr(workspace), int(workspace_bytes),
+                                             _ptr(o_res), _ptr(workspace), int(workspace_bytes),
                                              _stream(stream)),
            "fa_bwd_blocksparse")
+
+
+def _ws_bytes(workspace, workspace_bytes):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return int(workspace_bytes)
+
+
+def fa_bwd_prepare(o, o_res, lse, dout, workspace, workspace_bytes=None, stream=None):
+    B, H, N, d = _dims(o)
+    _check(load_library().fa_bwd_prepare(_ptr(o), _ptr(o_res), _ptr(lse), _ptr(dout), B, H, N, d,
+                                         _dtype_code(o), _ptr(workspace),
+                                         _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_bwd_prepare")
+
+
+def fa_bwd_main(q, k, v, dout, dk, dv, scale, causal=False, kv_len=None, block_mask=None,
+                workspace=None, workspace_bytes=None, stream=None):
+    B, H, N, d = _dims(q)
+    _check(load_library().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv),
+                                      B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q),
+                                      _ptr(kv_len), _ptr(block_mask), _ptr(workspace),
+                                      _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_bwd_main")
+
+
+def fa_bwd_finish(dq, workspace, workspace_bytes=None, stream=None):
+    B, H, N, d = _dims(dq)
+    _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, _dtype_code(dq), _ptr(workspace),
+                                        _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_bwd_finish")
 
 
 def fa_get_device_error(stream=None) -> int:

@@ -9,23 +9,27 @@ from . import _binding as B
 
 
 def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None,
-                      stream=None):
-    """O [B,H,N,d] and LSE [B,H,N] fp32 of exact attention (device tensors)."""
+                      return_residual=False, stream=None):
+    """O [B,H,N,d] and LSE [B,H,N] fp32 of exact attention (device tensors).
+
+    With return_residual=True also returns O's rounding residual (same dtype),
+    which attention_backward uses for a more accurate D = rowsum(dO * O)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    o_res = torch.empty_like(q) if return_residual else None
     if block_mask is not None:
-        B.fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, stream=stream)
-    elif kv_len is not None:
-        B.fa_fwd_ex(q, k, v, o, lse, scale, causal, kv_len, stream=stream)
+        B.fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, o_res=o_res, stream=stream)
+    elif kv_len is not None or o_res is not None:
+        B.fa_fwd_ex(q, k, v, o, lse, scale, causal, kv_len, o_res=o_res, stream=stream)
     else:
         B.fa_fwd(q, k, v, o, lse, scale, causal, stream=stream)
-    return o, lse
+    return (o, lse, o_res) if return_residual else (o, lse)
 
 
 def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=None,
-                       block_mask=None, workspace=None, stream=None):
+                       block_mask=None, o_res=None, workspace=None, stream=None):
     """dQ, dK, dV [B,H,N,d] of exact attention (device tensors)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
@@ -37,9 +41,9 @@ def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=N
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     if block_mask is not None:
-        B.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, workspace,
-                             stream=stream)
+        B.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, o_res=o_res,
+                             workspace=workspace, stream=stream)
     else:
-        B.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, kv_len, workspace,
-                 stream=stream)
+        B.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, kv_len, o_res=o_res,
+                 workspace=workspace, stream=stream)
     return dq, dk, dv

@@ -1,0 +1,524 @@
+// bwd_kernel.cuh -- backward attention kernels for sm_103a.
+//
+// The backward recomputes the probabilities tile by tile from Q, K and the
+// forward's log-sum-exp instead of storing them ("Flash Attention:
+// revolutionizing transformer efficiency", key idea 2, Recomputation). For
+// a key tile j and a query tile i, with P = exp(scale Q_i K_j^T - LSE_i):
+//   dV_j += P^T dO_i            dP = dO_i V_j^T
+//   dS    = P o (dP - D_i),     D_i = rowsum(dO_i o O_i)
+//   dK_j += scale dS^T Q_i      dQ_i += scale dS K_j
+//
+// Three kernels:
+//   bwd_pre_kernel   D_i and LSE_i * log2(e) per query row (padded to whole
+//                    128-row tiles; pad rows get D = 0, LSE = +inf so P = 0)
+//                    and zeroes the fp32 dQ accumulator. D_i = dO_i . O_i
+//                    uses O plus its rounding residual when the forward
+//                    wrote one: with bf16 O alone the rounding of O moves
+//                    D_i by up to ~0.05 at d = 128, which reaches dQ and dK.
+//   bwd_main_kernel  one CTA per 128-key tile of one (batch, head); K_j, V_j
+//                    stay in shared memory, dK_j and dV_j stay in TMEM, and
+//                    the CTA loops over the query tiles that see key tile j.
+//                    The scores are computed transposed (keys on TMEM lanes)
+//                    so P^T and dS^T are row-local to one thread per key.
+//   bwd_dq_kernel    dQ accumulator (fp32) -> dQ (fp16/bf16).
+//
+// Main-kernel roles (384 threads):
+//   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
+//                   query tile i through a two-stage ring.
+//   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
+//   warps 4..7      thread r owns key r: P^T row -> TMEM (16-bit), dS^T row
+//                   -> shared memory (16-bit, scale folded in, computed from
+//                   the fp32 P); final dK, dV.
+//   warps 8..11     read the dQ partial from TMEM and add it to the fp32
+//                   accumulator (d = 128: thread r owns head-dim channel r of
+//                   the transposed partial; d = 64: thread r owns query r).
+// TMEM columns: dK [0,D), dV [D,2D), S^T [2D,2D+128) (P^T aliases its first
+// 64 columns), dP^T [2D+128, 2D+256) (the dQ partial reuses it once dS is out).
+#pragma once
+#include "common.cuh"
+
+namespace fa {
+
+struct BwdArgs {
+  void *dq, *dk, *dv;
+  const void *o, *dout;
+  const void *o_res;  // rounding residual of O (same 16-bit type) or null
+  const float *lse;
+  float *lse_l2;    // [BH, nqt*128]
+  float *delta;     // [BH, nqt*128]
+  float *dq_acc;    // [BH, nqt*128, D]
+  const int32_t *kv_len;
+  const uint8_t *block_mask;
+  int H, N, nqt, nkt;
+  float scale, scale_log2;
+};
+
+// 1-D bulk copy global -> shared, completion as transaction bytes on bar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- pre
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long rows_pad) {
+  constexpr int LPR = D / 8;         // lanes per row (8 elements each)
+  constexpr int RPW = 32 / LPR;      // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPR, grp = lane / LPR;
+  const long long tile_rows = static_cast<long long>(a.nqt) * 128;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  for (long long base = w0 * RPW; base < rows_pad; base += warps * RPW) {
+    const long long row = base + grp;
+    const bool live = row < rows_pad;
+    float acc = 0.f;
+    long long bh = 0, i = 0;
+    if (live) {
+      bh = row / tile_rows;
+      i = row % tile_rows;
+      if (i < a.N) {
+        const size_t off = (static_cast<size_t>(bh) * a.N + i) * D + sub * 8;
+        const uint4 o4 = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.o) + off);
+        const uint4 g4 =
+            *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + off);
+        uint4 r4 = make_uint4(0u, 0u, 0u, 0u);
+        if (a.o_res != nullptr)
+          r4 = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.o_res) + off);
+        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+        const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc = fmaf(unpack_lo<BF16>(ow[k]) + unpack_lo<BF16>(rw[k]), unpack_lo<BF16>(gw[k]), acc);
+          acc = fmaf(unpack_hi<BF16>(ow[k]) + unpack_hi<BF16>(rw[k]), unpack_hi<BF16>(gw[k]), acc);
+        }
+      }
+      float4 *z = reinterpret_cast<float4 *>(a.dq_acc + row * D + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (live && sub == 0) {
+      a.delta[row] = acc;
+      float l2 = INFINITY;
+      if (i < a.N) {
+        const float l = a.lse[static_cast<size_t>(bh) * a.N + i];
+        if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+      }
+      a.lse_l2[row] = l2;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- dq convert
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdArgs a, long long n_vec4, int D) {
+  // n_vec4 = BH * N * D / 4 output groups of 4 elements
+  const long long tile_rows = static_cast<long long>(a.nqt) * 128;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_vec4;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long e = g * 4;
+    const long long row = e / D, c = e % D;
+    const long long bh = row / a.N, i = row % a.N;
+    const float4 v = *reinterpret_cast<const float4 *>(a.dq_acc + (bh * tile_rows + i) * D + c);
+    uint2 out;
+    out.x = pack2<BF16>(v.x, v.y);
+    out.y = pack2<BF16>(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.dq) + e) = out;
+  }
+}
+
+// ----------------------------------------------------------------- main
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kKB = D / 64;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;         // 2 stages
+  static constexpr int kdOOff = kQOff + 2 * kTileBytes;    // 2 stages
+  static constexpr int kdSOff = kdOOff + 2 * kTileBytes;   // 128 keys x 128 queries bf16
+  static constexpr int kLseOff = kdSOff + 32768;           // 2 stages x 128 fp32
+  static constexpr int kDeltaOff = kLseOff + 1024;         // 2 stages x 128 fp32
+  static constexpr int kBarOff = kDeltaOff + 1024;
+  static constexpr int kBKV = 0, kBQF = 1, kBQE = 3, kBSF = 5, kBDPF = 6, kBPR = 7 /* x2 */,
+                       kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13, kBDSF = 14,
+                       kNumBars = 15;
+  // d = 128: the dQ partial is computed transposed (dQ^T = K^T dS^T, TMEM
+  // lane = head-dim channel, column = query) so one warp's reduction into
+  // the fp32 accumulator covers 32 consecutive channels of a row: a whole
+  // 128-byte line per instruction instead of 32 scattered 16-byte pieces.
+  static constexpr bool kDqT = (D == 128);
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColDP + 128 <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Next kept query tile >= from for key tile kt (block-sparse column scan).
+__device__ __forceinline__ int next_kept(const uint8_t *mask, int nkt, int nqt, int kt, int from) {
+  int i = from;
+  while (i < nqt && mask[static_cast<size_t>(i) * nkt + kt] == 0) ++i;
+  return i;
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+__global__ void __launch_bounds__(384, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (sbase & 1023u) {  // the swizzled tiles need a 1 KB aligned base
+    if (tid == 0) atomicOr(&g_fa_device_error, kDevErrTimeout);
+    return;
+  }
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  volatile uint32_t *abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
+
+  const int bh = blockIdx.x / a.nkt;
+  const int kt = blockIdx.x % a.nkt;  // causal: low key tiles carry the most work, run first
+  const int b = bh / a.H;
+  int kvl = a.N;
+  if (a.kv_len != nullptr) {
+    const int v = a.kv_len[b];
+    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
+  }
+  // query tiles that see this key tile: [q_begin, nqt), filtered by the mask
+  const bool key_tile_live = kt * 128 < kvl;
+  const int q_begin = CAUSAL ? kt : 0;
+  int n_iter = 0;
+  if (key_tile_live) {
+    if (SPARSE) {
+      for (int i = 0; i < a.nqt; ++i) n_iter += a.block_mask[static_cast<size_t>(i) * a.nkt + kt] != 0;
+    } else {
+      n_iter = a.nqt - q_begin;
+    }
+  }
+
+  if (tid == 0) {
+    mbar_init(bar(C::kBKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kBQF + s), 1);
+      mbar_init(bar(C::kBQE + s), 1);
+    }
+    mbar_init(bar(C::kBSF), 1);
+    mbar_init(bar(C::kBDPF), 1);
+    mbar_init(bar(C::kBPR), 128);
+    mbar_init(bar(C::kBPR + 1), 128);
+    mbar_init(bar(C::kBDV), 1);
+    mbar_init(bar(C::kBDSR), 128);
+    mbar_init(bar(C::kBDQF), 1);
+    mbar_init(bar(C::kBDQE), 128);
+    mbar_init(bar(C::kBFIN), 1);
+    mbar_init(bar(C::kBDSF), 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const long long tile_rows = static_cast<long long>(a.nqt) * 128;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_iter > 0) {
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBKV), 2 * C::kTileBytes);
+      for (int kb = 0; kb < C::kKB; ++kb) {
+        tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKV), kb * 64, kt * 128, bh, pol_kv);
+        tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBKV), kb * 64, kt * 128, bh, pol_kv);
+      }
+      int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+      int issued = 0;
+      for (int u = 0; u < n_iter; ++u) {
+        const int st = u & 1;
+        if (!mbar_wait(bar(C::kBQE + st), ((u >> 1) & 1) ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBQF + st), 2 * C::kTileBytes + 1024);
+        for (int kb = 0; kb < C::kKB; ++kb) {
+          tma_load_3d_hint(sbase + C::kQOff + st * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQF + st),
+                           kb * 64, qi * 128, bh, pol_q);
+          tma_load_3d_hint(sbase + C::kdOOff + st * C::kTileBytes + kb * 16384, &tm_do,
+                           bar(C::kBQF + st), kb * 64, qi * 128, bh, pol_q);
+        }
+        const long long r0 = bh * tile_rows + static_cast<long long>(qi) * 128;
+        bulk_load(sbase + C::kLseOff + st * 512, a.lse_l2 + r0, 512, bar(C::kBQF + st));
+        bulk_load(sbase + C::kDeltaOff + st * 512, a.delta + r0, 512, bar(C::kBQF + st));
+        issued = u + 1;
+        qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(bar(C::kBKV), 0, abort_flag);
+        for (int u = max(0, issued - 2); u < issued; ++u)
+          mbar_wait_drain(bar(C::kBQF + (u & 1)), (u >> 1) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t kIdSS = idesc_f16(BF16, 128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdKV = idesc_f16(BF16, 128, D, false, true);      // dK, dV
+      constexpr uint32_t kIdQ = C::kDqT ? idesc_f16(BF16, 128, 128, true, true)  // dQ^T
+                                        : idesc_f16(BF16, 128, D, true, true);   // dQ
+      const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sDS = sbase + C::kdSOff;
+      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag);
+      for (int u = 0; ok && u < n_iter; ++u) {
+        const int st = u & 1;
+        const uint32_t sQ = sbase + C::kQOff + st * C::kTileBytes;
+        const uint32_t sdO = sbase + C::kdOOff + st * C::kTileBytes;
+        if (!mbar_wait(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
+        // S^T region is free once the previous dV MMA has read P^T from it
+        if (u > 0 && !mbar_wait(bar(C::kBDV), (u - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {  // S^T = K_j Q_i^T
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
+                 kIdSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBSF));
+        // dP^T region is free once the previous dQ partial has been read out
+        if (u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
+                 kIdSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBDPF));
+        // dV_j += P^T dO_i, P^T read from TMEM, one 64-query half at a time
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!mbar_wait(bar(C::kBPR + h), u & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + (4 * h + ks) * 8,
+                   sdesc_sw128(sdO + (4 * h + ks) * 2048, 16384, 1024), kIdKV,
+                   (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBDV));
+        if (!mbar_wait(bar(C::kBDSR), u & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // dQ first, so its read-out overlaps the dK MMA
+        if constexpr (C::kDqT) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
+            mma_ss(tmem + C::kColDP, sdesc_sw128(sK + ks * 2048, 16384, 1024),
+                   sdesc_sw128(sDS + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dQ_i = dS K_j (dS read MN-major from the dS^T buffer)
+            mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
+                   sdesc_sw128(sK + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBDQF));
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
+          mma_ss(tmem + C::kColDK,
+                 sdesc_sw128(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(sQ + ks * 2048, 16384, 1024), kIdKV, (u > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(C::kBDSF));
+        mma_commit(bar(C::kBQE + st));
+      }
+      mma_commit(bar(C::kBFIN));
+      mbar_wait_drain(bar(C::kBFIN), 0, abort_flag);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P^T and dS^T
+    const int r = tid - 128;  // key row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int key = kt * 128 + r;
+    const bool key_live = key < kvl;
+    const float sl2 = a.scale_log2, scale = a.scale;
+    const uint32_t sDS = sbase + C::kdSOff;
+    bool ok = true;
+    int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+    for (int u = 0; u < n_iter; ++u) {
+      const int st = u & 1;
+      const float *lse_s = reinterpret_cast<const float *>(smem + C::kLseOff + st * 512);
+      const float *dl_s = reinterpret_cast<const float *>(smem + C::kDeltaOff + st * 512);
+      if (!mbar_wait_warp(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(C::kBSF), u & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      // causal: query c of this tile sees key r iff qi*128 + c >= key
+      const int cmin = CAUSAL ? (key - qi * 128) : -1;
+      // Two halves of 64 queries: P (fp32, kept in registers for dS) ->
+      // P^T (16-bit) into TMEM columns [32h, 32h+32) of the S^T region (the
+      // scores there were already read), then dS^T of the same queries.
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float p[64];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t sr[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h + c0, sr);
+          tmem_wait_ld();
+          reg_fence_32(sr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 64 * h + c0 + i;
+            const float x = ex2_approx(fmaf(__uint_as_float(sr[i]), sl2, -lse_s[c]));
+            p[c0 + i] = (!key_live || c < cmin) ? 0.f : x;
+          }
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack2<BF16>(p[2 * (c0 + i)], p[2 * (c0 + i) + 1]);
+          tmem_st_32x32b_x16(tmem + lane_addr + C::kColS + 32 * h + c0, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBPR + h));
+        if (h == 0) {
+          if (!mbar_wait_warp(bar(C::kBDPF), u & 1, abort_flag)) { ok = false; break; }
+          // the previous dQ/dK MMAs must be done reading dS before it is rewritten
+          if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t dr[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h + c0, dr);
+          tmem_wait_ld();
+          reg_fence_32(dr);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int c = 64 * h + c0 + i;
+            const float ds0 = scale * p[c0 + i] * (__uint_as_float(dr[i]) - dl_s[c]);
+            const float ds1 = scale * p[c0 + i + 1] * (__uint_as_float(dr[i + 1]) - dl_s[c + 1]);
+            w[i / 2] = pack2<BF16>(ds0, ds1);
+          }
+          // row r of the dS^T tile, queries 64h+c0 .. +31 = 4 16-byte chunks of
+          // the 128-byte row in region h, swizzled by (r & 7)
+          const uint32_t rowb = sDS + h * 16384 + r * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t chunk = ((c0 >> 3) + v) ^ (r & 7);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + chunk * 16),
+                         "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3])
+                         : "memory");
+          }
+        }
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBDSR));
+      qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+    }
+    // ---- dK, dV epilogue
+    bool have = ok && n_iter > 0;
+    if (have) {
+      have = mbar_wait_warp(bar(C::kBFIN), 0, abort_flag);
+      tc_fence_after();
+    }
+    const size_t orow = (static_cast<size_t>(bh) * a.N + static_cast<size_t>(key)) * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      uint16_t *dst = static_cast<uint16_t *>(which == 0 ? a.dk : a.dv) + orow;
+      const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        if (have) {
+          tmem_ld_32x32b_x32(tmem + lane_addr + col + c0, v);
+          tmem_wait_ld();
+          reg_fence_32(v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (key < a.N) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ partials
+    const int r = tid - 256;  // query row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+    for (int u = 0; u < n_iter; ++u) {
+      if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
+      tc_fence_after();
+      if constexpr (C::kDqT) {
+        // thread r holds channel r of the 128 queries of this tile
+        float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128) * D + r;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + c0, v);
+          tmem_wait_ld();
+          reg_fence_32(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) atomicAdd(acc + (c0 + i) * D, __uint_as_float(v[i]));
+        }
+      } else {
+        float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + c0, v);
+          tmem_wait_ld();
+          reg_fence_32(v);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            atomicAdd(reinterpret_cast<float4 *>(acc + c0 + i),
+                      make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kBDQE));
+      qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

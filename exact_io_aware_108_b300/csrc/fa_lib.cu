@@ -15,6 +15,7 @@
 
 #include "fa.h"
 #include "fwd_kernel.cuh"
+#include "bwd_kernel.cuh"
 
 namespace {
 
@@ -146,7 +147,7 @@ fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int N, int d, float scale, int causal, fa_dtype dt, const int32_t *kv_len,
-                   const uint8_t *block_mask, bool sparse, void *stream) {
+                   const uint8_t *block_mask, bool sparse, void *o_res, void *stream) {
   Shape s;
   fa_status r = check_common(B, H, N, d, scale, dt, &s);
   if (r != FA_OK) return r;
@@ -159,12 +160,15 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   }
   if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
     return fail(FA_ERR_INVALID_ARG, "kv_len is not 4-byte aligned");
+  if (o_res != nullptr && !aligned16(o_res))
+    return fail(FA_ERR_INVALID_ARG, "o_res is not 16-byte aligned");
   CUtensorMap tq, tk, tv;
   if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
   if ((r = make_tile_map(&tk, k, dt, N, s.BH, d, "k")) != FA_OK) return r;
   if ((r = make_tile_map(&tv, v, dt, N, s.BH, d, "v")) != FA_OK) return r;
   fa::FwdArgs a;
   a.o = o;
+  a.o_res = o_res;
   a.lse = lse;
   a.kv_len = kv_len;
   a.block_mask = block_mask;
@@ -186,16 +190,141 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   return ok();
 }
 
+// Workspace: LSE*log2(e) and D per query row, padded to whole 128-row tiles,
+// then the fp32 dQ accumulator over the same padded rows.
+size_t padded_rows(int B, int H, int N) {
+  return static_cast<size_t>(B) * H * static_cast<size_t>((N + 127) / 128) * 128;
+}
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 size_t fa_bwd_ws_bytes(int B, int H, int N, int d) {
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return up(rows * 4) + up(rows * static_cast<size_t>(d) * 4);
+  const size_t rows = padded_rows(B, H, N);
+  return 2 * up256(rows * 4) + up256(rows * static_cast<size_t>(d) * 4);
 }
 
-fa_status bwd_impl(const void *, const void *, const void *, const void *, const float *,
-                   const void *, void *, void *, void *, int, int, int, int, float, int, fa_dtype,
-                   const int32_t *, const uint8_t *, bool, void *, size_t, void *) {
-  return fail(FA_ERR_UNSUPPORTED, "backward not built yet");
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+fa_status launch_bwd_main_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &tdo, const fa::BwdArgs &a, int grid, cudaStream_t st) {
+  auto kern = fa::bwd_main_kernel<D, BF16, CAUSAL, SPARSE>;
+  constexpr int smem = fa::BwdCfg<D>::kSmemBytes;
+  cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+  kern<<<grid, 384, smem, st>>>(tq, tk, tv, tdo, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+  return FA_OK;
+}
+
+enum BwdPhase : unsigned { kPrepare = 1u, kMain = 2u, kFinish = 4u, kAll = 7u };
+
+template <int D, bool BF16>
+fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const fa::BwdArgs &a, long long rows_pad,
+                       long long n_vec4, int grid, bool causal, bool sparse, unsigned phases,
+                       cudaStream_t st) {
+  cudaError_t e;
+  if (phases & kPrepare) {
+    constexpr int rows_per_block = 8 * (32 / (D / 8));
+    long long pre_blocks = (rows_pad + rows_per_block - 1) / rows_per_block;
+    if (pre_blocks > 148 * 16) pre_blocks = 148 * 16;
+    fa::bwd_pre_kernel<D, BF16><<<static_cast<int>(pre_blocks), 256, 0, st>>>(a, rows_pad);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "bwd prepare launch");
+  }
+  if (phases & kMain) {
+    fa_status r;
+    if (sparse)
+      r = launch_bwd_main_t<D, BF16, false, true>(tq, tk, tv, tdo, a, grid, st);
+    else if (causal)
+      r = launch_bwd_main_t<D, BF16, true, false>(tq, tk, tv, tdo, a, grid, st);
+    else
+      r = launch_bwd_main_t<D, BF16, false, false>(tq, tk, tv, tdo, a, grid, st);
+    if (r != FA_OK) return r;
+  }
+  if (phases & kFinish) {
+    long long dq_blocks = (n_vec4 + 255) / 256;
+    if (dq_blocks > 148 * 16) dq_blocks = 148 * 16;
+    fa::bwd_dq_kernel<BF16><<<static_cast<int>(dq_blocks), 256, 0, st>>>(a, n_vec4, D);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "bwd finish launch");
+  }
+  return FA_OK;
+}
+
+fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                   float scale, int causal, fa_dtype dt, const int32_t *kv_len,
+                   const uint8_t *block_mask, bool sparse, const void *o_res, void *workspace,
+                   size_t ws_bytes, void *stream, unsigned phases = kAll) {
+  Shape s;
+  fa_status r = check_common(B, H, N, d, scale, dt, &s);
+  if (r != FA_OK) return r;
+  // each phase reads/writes only some of the tensors
+  if (phases & kPrepare) {
+    r = check_ptrs({{o, "o"}, {lse, "lse"}, {dout, "dout"}});
+    if (r != FA_OK) return r;
+  }
+  if (phases & kMain) {
+    r = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {dout, "dout"}, {dk, "dk"}, {dv, "dv"}});
+    if (r != FA_OK) return r;
+  }
+  if (phases & kFinish) {
+    r = check_ptrs({{dq, "dq"}});
+    if (r != FA_OK) return r;
+  }
+  r = check_ptrs({{workspace, "workspace"}});
+  if (r != FA_OK) return r;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(FA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = fa_bwd_ws_bytes(B, H, N, d);
+  if (ws_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  if (sparse && block_mask == nullptr) return fail(FA_ERR_INVALID_ARG, "block_mask is null");
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "kv_len is not 4-byte aligned");
+  if (o_res != nullptr && !aligned16(o_res))
+    return fail(FA_ERR_INVALID_ARG, "o_res is not 16-byte aligned");
+  CUtensorMap tq, tk, tv, tdo;
+  if (phases & kMain) {
+    if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
+    if ((r = make_tile_map(&tk, k, dt, N, s.BH, d, "k")) != FA_OK) return r;
+    if ((r = make_tile_map(&tv, v, dt, N, s.BH, d, "v")) != FA_OK) return r;
+    if ((r = make_tile_map(&tdo, dout, dt, N, s.BH, d, "dout")) != FA_OK) return r;
+  }
+  const size_t rows = padded_rows(B, H, N);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  fa::BwdArgs a;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.o = o;
+  a.o_res = o_res;
+  a.dout = dout;
+  a.lse = lse;
+  a.lse_l2 = reinterpret_cast<float *>(ws);
+  a.delta = reinterpret_cast<float *>(ws + up256(rows * 4));
+  a.dq_acc = reinterpret_cast<float *>(ws + 2 * up256(rows * 4));
+  a.kv_len = kv_len;
+  a.block_mask = block_mask;
+  a.H = H;
+  a.N = N;
+  a.nqt = s.nqt;
+  a.nkt = s.nqt;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long long rows_pad = static_cast<long long>(rows);
+  const long long n_vec4 = s.BH * static_cast<long long>(N) * d / 4;
+  const int grid = static_cast<int>(s.BH * s.nqt);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool c = causal != 0;
+  if (d == 64)
+    r = dt == FA_BF16 ? launch_bwd_d<64, true>(tq, tk, tv, tdo, a, rows_pad, n_vec4, grid, c, sparse, phases, st)
+                      : launch_bwd_d<64, false>(tq, tk, tv, tdo, a, rows_pad, n_vec4, grid, c, sparse, phases, st);
+  else
+    r = dt == FA_BF16 ? launch_bwd_d<128, true>(tq, tk, tv, tdo, a, rows_pad, n_vec4, grid, c, sparse, phases, st)
+                      : launch_bwd_d<128, false>(tq, tk, tv, tdo, a, rows_pad, n_vec4, grid, c, sparse, phases, st);
+  if (r != FA_OK) return r;
+  return ok();
 }
 
 }  // namespace
@@ -205,20 +334,21 @@ extern "C" {
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                  int N, int d, float scale, int causal, fa_dtype dtype, void *stream) {
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nullptr, nullptr, false,
-                  stream);
+                  nullptr, stream);
 }
 
 fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                     int N, int d, float scale, int causal, fa_dtype dtype, const int32_t *kv_len,
-                    void *stream) {
+                    void *o_res, void *stream) {
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
-                  stream);
+                  o_res, stream);
 }
 
 fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int N, int d, float scale, fa_dtype dtype,
-                             const uint8_t *block_mask, void *stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, 0, dtype, nullptr, block_mask, true, stream);
+                             const uint8_t *block_mask, void *o_res, void *stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, 0, dtype, nullptr, block_mask, true, o_res,
+                  stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -228,19 +358,43 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                  const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, const int32_t *kv_len, void *workspace,
-                 size_t workspace_bytes, void *stream) {
+                 float scale, int causal, fa_dtype dtype, const int32_t *kv_len, const void *o_res,
+                 void *workspace, size_t workspace_bytes, void *stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, dtype, kv_len,
-                  nullptr, false, workspace, workspace_bytes, stream);
+                  nullptr, false, o_res, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
                              int B, int H, int N, int d, float scale, fa_dtype dtype,
-                             const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
-                             void *stream) {
+                             const uint8_t *block_mask, const void *o_res, void *workspace,
+                             size_t workspace_bytes, void *stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, 0, dtype, nullptr,
-                  block_mask, true, workspace, workspace_bytes, stream);
+                  block_mask, true, o_res, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_prepare(const void *o, const void *o_res, const float *lse, const void *dout,
+                         int B, int H, int N, int d, fa_dtype dtype, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  return bwd_impl(nullptr, nullptr, nullptr, o, lse, dout, nullptr, nullptr, nullptr, B, H, N, d,
+                  1.0f, 0, dtype, nullptr, nullptr, false, o_res, workspace, workspace_bytes,
+                  stream, kPrepare);
+}
+
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
+                      void *dv, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, const int32_t *kv_len, const uint8_t *block_mask,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, k, v, nullptr, nullptr, dout, nullptr, dk, dv, B, H, N, d, scale,
+                  block_mask ? 0 : causal, dtype, kv_len, block_mask, block_mask != nullptr,
+                  nullptr, workspace, workspace_bytes, stream, kMain);
+}
+
+fa_status fa_bwd_finish(void *dq, int B, int H, int N, int d, fa_dtype dtype, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  return bwd_impl(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr, B, H,
+                  N, d, 1.0f, 0, dtype, nullptr, nullptr, false, nullptr, workspace,
+                  workspace_bytes, stream, kFinish);
 }
 
 fa_status fa_get_device_error(void *stream) {

@@ -23,9 +23,11 @@
 // Online softmax in base 2: x = s * scale * log2(e); p = 2^(x - m);
 // l <- 2^(m_old - m) l + sum p; O <- 2^(m_old - m) O + P V
 // (softmax decomposition and merger, section "The Math Behind Flash
-// Attention"). m is only moved when the row max grows by more than 8 (a
-// factor 256), so most tiles need no O rescale; O, l and the final LSE all
-// use the same m, so the result is unchanged.
+// Attention"). m is the exact running row max, so the largest probability of
+// a row is exactly 1 when it is rounded to 16 bits for the P V product; O is
+// rescaled in TMEM whenever any row of the warp sees a new max. (Letting m lag
+// the max, to skip rescales, rounds the dominant probability too: for sharp
+// bf16 softmax that doubled the error of O and of D = rowsum(dO * O).)
 #pragma once
 #include "common.cuh"
 
@@ -33,6 +35,7 @@ namespace fa {
 
 struct FwdArgs {
   void *o;
+  void *o_res;               // [B,H,N,D] rounding residual of O, or null
   float *lse;
   const int32_t *kv_len;     // [B] or null
   const uint8_t *block_mask; // [nkt, nkt] or null
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(256, 1)
         mx3 = fmaxf(mx3, s[c + 3]);
       }
       const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = (mxs > m + 8.0f) ? mxs : m;
+      const float m_new = fmaxf(m, mxs);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
@@ -348,15 +351,25 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
-      uint32_t pk[16];
+      uint32_t pk[16], rk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      for (int i = 0; i < 16; ++i) {
+        const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+        pk[i] = pack2<BF16>(x0, x1);
+        rk[i] = pack2<BF16>(x0 - unpack_lo<BF16>(pk[i]), x1 - unpack_hi<BF16>(pk[i]));
+      }
       if (q_row < a.N) {
         uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        if (a.o_res != nullptr) {
+          uint4 *dr = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.o_res) +
+                                                (orow - static_cast<uint16_t *>(a.o)) + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dr[v] = make_uint4(rk[4 * v], rk[4 * v + 1], rk[4 * v + 2], rk[4 * v + 3]);
+        }
       }
     }
     if (q_row < a.N)

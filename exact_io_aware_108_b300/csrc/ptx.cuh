@@ -6,6 +6,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 namespace fa {
 
@@ -213,6 +214,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Low / high 16-bit element of a packed pair -> fp32 (exact).
+template <bool BF16>
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+  if constexpr (BF16)
+    return __uint_as_float(w << 16);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+template <bool BF16>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+  if constexpr (BF16)
+    return __uint_as_float(w & 0xFFFF0000u);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
 }  // namespace fa

@@ -87,13 +87,20 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  fa_dtype dtype, void *stream);
 
 /*
- * fa_fwd with key padding: kv_len is a DEVICE int32 [B] array (or NULL for
- * none); keys j >= kv_len[b] are masked for all queries of batch b. Values
- * above N act as N; values below 1 mask every key of that batch.
+ * fa_fwd with key padding and an optional output residual.
+ *   kv_len  DEVICE int32 [B] array, or NULL for none; keys j >= kv_len[b] are
+ *           masked for all queries of batch b. Values above N act as N;
+ *           values below 1 mask every key of that batch.
+ *   o_res   DEVICE [B,H,N,d] array of the same 16-bit type, or NULL. When
+ *           given, it receives the rounding residual of O: the fp32 result
+ *           minus its 16-bit rounding, itself rounded to 16 bits, so that
+ *           o + o_res carries about twice the precision of o. The backward
+ *           uses it for D = rowsum(dO * O); with bf16 alone, the rounding of O
+ *           moves D by up to ~0.05 at d = 128, which reaches dQ and dK.
  */
 fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                     int B, int H, int N, int d, float scale, int causal,
-                    fa_dtype dtype, const int32_t *kv_len, void *stream);
+                    fa_dtype dtype, const int32_t *kv_len, void *o_res, void *stream);
 
 /*
  * Block-sparse forward (FlashAttention abstract: "We also extend
@@ -101,15 +108,19 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
  * array [nb, nb], nb = ceil(N / 128), row = query tile, column = key tile,
  * nonzero = keep, shared by all (b, h). Masked tiles are neither loaded nor
  * multiplied; inside a kept tile attention is dense and non-causal.
+ * o_res as in fa_fwd_ex (NULL for none).
  */
 fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o,
                              float *lse, int B, int H, int N, int d, float scale,
-                             fa_dtype dtype, const uint8_t *block_mask, void *stream);
+                             fa_dtype dtype, const uint8_t *block_mask, void *o_res,
+                             void *stream);
 
 /*
  * Bytes of device workspace fa_bwd / fa_bwd_blocksparse need for these
- * sizes: fp32 D = rowsum(dO * O) [B,H,N] and an fp32 dQ accumulator
- * [B,H,N,d], each rounded up to 256 bytes. Returns 0 for invalid sizes.
+ * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
+ * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ
+ * accumulator [R, d], each rounded up to 256 bytes. Returns 0 for invalid
+ * sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -122,21 +133,46 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   dQ = scale dS K,  dK = scale dS^T Q.
  *   q, k, v, o, dout [B,H,N,d] in; lse [B,H,N] in (from the forward with the
  *   same arguments); dq, dk, dv [B,H,N,d] out; kv_len as in fa_fwd_ex.
+ *   o_res: the residual fa_fwd_ex wrote for this O, or NULL (then D uses O
+ *   alone).
  *   workspace: DEVICE memory of at least fa_bwd_workspace_size(B,H,N,d)
  *   bytes, 256-byte aligned, owned by the caller, contents ignored on entry.
+ * dK and dV are deterministic; dQ sums the key tiles with fp32 atomics, so
+ * its last bits may vary between runs.
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  const float *lse, const void *dout, void *dq, void *dk, void *dv,
                  int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
-                 const int32_t *kv_len, void *workspace, size_t workspace_bytes,
-                 void *stream);
+                 const int32_t *kv_len, const void *o_res, void *workspace,
+                 size_t workspace_bytes, void *stream);
 
 /* Block-sparse backward: fa_bwd with the block mask of fa_fwd_blocksparse. */
 fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
                              const float *lse, const void *dout, void *dq, void *dk,
                              void *dv, int B, int H, int N, int d, float scale,
-                             fa_dtype dtype, const uint8_t *block_mask, void *workspace,
-                             size_t workspace_bytes, void *stream);
+                             fa_dtype dtype, const uint8_t *block_mask, const void *o_res,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The three launches fa_bwd makes, in order, for callers that schedule or
+ * time them separately (fa_bwd == prepare; main; finish on one stream, same
+ * workspace). Arguments mean what they mean for fa_bwd / fa_bwd_blocksparse.
+ *   fa_bwd_prepare  D = rowsum(dO * (O + o_res)) and LSE * log2(e) into the
+ *                   workspace; zeroes the workspace's fp32 dQ accumulator.
+ *   fa_bwd_main     one CTA per 128-key tile: dK and dV (written directly),
+ *                   dQ partials added into the accumulator. block_mask NULL
+ *                   means dense/causal (causal applies only then).
+ *   fa_bwd_finish   dQ accumulator -> dq (fp16/bf16).
+ */
+fa_status fa_bwd_prepare(const void *o, const void *o_res, const float *lse, const void *dout,
+                         int B, int H, int N, int d, fa_dtype dtype, void *workspace,
+                         size_t workspace_bytes, void *stream);
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
+                      void *dv, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, const int32_t *kv_len, const uint8_t *block_mask,
+                      void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_bwd_finish(void *dq, int B, int H, int N, int d, fa_dtype dtype, void *workspace,
+                        size_t workspace_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error flag set by

@@ -37,7 +37,8 @@ def test_status_strings_and_version():
 def test_workspace_size():
     def up(x):
         return (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == up(2 * 3 * 300 * 4) + up(2 * 3 * 300 * 64 * 4)
+    rows = 2 * 3 * 384  # query rows padded to whole 128-row tiles
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * up(rows * 4) + up(rows * 64 * 4)
     assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
@@ -70,22 +71,25 @@ def test_bwd_rejects_bad_arguments():
     c = ctypes.c_float(0.125)
     args = [FAKE] * 9
     # workspace too small
-    st = lib.fa_bwd(*args, 1, 1, 128, 64, c, 0, 0, None, FAKE, 16, None)
+    st = lib.fa_bwd(*args, 1, 1, 128, 64, c, 0, 0, None, None, FAKE, 16, None)
     assert st == 1
     # null dq
     a2 = list(args)
     a2[6] = None
-    st = lib.fa_bwd(*a2, 1, 1, 128, 64, c, 0, 0, None, FAKE, 1 << 30, None)
+    st = lib.fa_bwd(*a2, 1, 1, 128, 64, c, 0, 0, None, None, FAKE, 1 << 30, None)
+    assert st == 1
+    # misaligned residual
+    st = lib.fa_bwd(*args, 1, 1, 128, 64, c, 0, 0, None, FAKE + 2, FAKE, 1 << 30, None)
     assert st == 1
     # block-sparse without a mask
-    st = lib.fa_bwd_blocksparse(*args, 1, 1, 128, 64, c, 0, None, FAKE, 1 << 30, None)
+    st = lib.fa_bwd_blocksparse(*args, 1, 1, 128, 64, c, 0, None, None, FAKE, 1 << 30, None)
     assert st == 1
 
 
 def test_blocksparse_rejects_missing_mask():
     lib = fa.load_library()
     st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
-                                None, None)
+                                None, None, None)
     assert st == 1
 
 

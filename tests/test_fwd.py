@@ -149,12 +149,13 @@ def _sample_rows(N, rng, n=48):
     "bert_b16_h16_n512_d64_f16_kvlen",
     "gpt2_b8_h12_n1024_d64_bf16_causal",
     "long_b8_h16_n4096_d128_bf16_causal",
+    "long_b4_h16_n8192_d128_bf16_causal",
     "long_b2_h16_n16384_d128_bf16_causal",
     "blocksparse_b2_h8_n16384_d64_f16",
 ])
 def test_fwd_full_size_sampled(name):
     """Full-size workload, same launch as the benchmark; sampled rows of a few
-    heads are checked against the oracle one by one."""
+    heads are checked against the oracle one by one, and one whole head."""
     w = inputs.WORKLOADS[name]
     t = inputs.make_workload(w, with_dout=False)
     o, lse = run_fwd(t["q"], t["k"], t["v"], w.scale, w.causal, t.get("kv_len"),
@@ -169,3 +170,10 @@ def test_fwd_full_size_sampled(name):
                                            w.causal, klb, t.get("block_mask"))
         check(f"O[{b},{h}]", o[b, h, rows], o_ref, TOL_O, t["q"].dtype)
         check(f"LSE[{b},{h}]", lse[b, h, rows], lse_ref, TOL_LSE, torch.float32)
+    b, h = w.B - 1, w.H - 1
+    kl = None if "kv_len" not in t else t["kv_len"][b:b + 1]
+    o_ref, lse_ref = ref.attn_fwd(t["q"][b:b + 1, h:h + 1], t["k"][b:b + 1, h:h + 1],
+                                  t["v"][b:b + 1, h:h + 1], w.scale, w.causal, kl,
+                                  t.get("block_mask"))
+    check(f"O[{b},{h}] whole head", o[b, h], o_ref[0, 0], TOL_O, t["q"].dtype)
+    check(f"LSE[{b},{h}] whole head", lse[b, h], lse_ref[0, 0], TOL_LSE, torch.float32)
