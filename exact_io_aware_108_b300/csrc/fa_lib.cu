@@ -124,10 +124,10 @@ cudaError_t set_smem(const void *kernel, int bytes) {
   return e;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
 fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
-  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE>;
+  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT>;
   constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
@@ -137,12 +137,21 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   return FA_OK;
 }
 
+template <int D, bool BF16, bool SPLIT>
+fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
+  if (sparse) return launch_fwd_t<D, BF16, false, true, SPLIT>(tq, tk, tv, a, grid, st);
+  if (causal) return launch_fwd_t<D, BF16, true, false, SPLIT>(tq, tk, tv, a, grid, st);
+  return launch_fwd_t<D, BF16, false, false, SPLIT>(tq, tk, tv, a, grid, st);
+}
+
+// The residual path (o_res given) also runs the split-probability P V
+// product, so that O, and with it D in the backward, is accurate.
 template <int D, bool BF16>
 fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
-  if (sparse) return launch_fwd_t<D, BF16, false, true>(tq, tk, tv, a, grid, st);
-  if (causal) return launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st);
-  return launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
+  if (a.o_res != nullptr) return launch_fwd_s<D, BF16, true>(tq, tk, tv, a, grid, causal, sparse, st);
+  return launch_fwd_s<D, BF16, false>(tq, tk, tv, a, grid, causal, sparse, st);
 }
 
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

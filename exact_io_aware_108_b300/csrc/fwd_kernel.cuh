@@ -74,7 +74,14 @@ struct FwdCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE>
+// SPLIT (the caller asked for O's rounding residual, i.e. for an O accurate
+// enough to form D = rowsum(dO * O) in the backward): each probability p is
+// sent to the tensor core as p_hi = bf16/f16(p) and p_lo = bf16/f16(p - p_hi),
+// and O += P_hi V + P_lo V, so O carries the rounding of P only to second
+// order. P_lo of tile t is written into the upper half of its own S buffer
+// (already read), and the MMA thread waits for P V of tile t to finish before
+// QK^T of tile t + 2 overwrites that buffer.
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -204,6 +211,13 @@ __global__ void __launch_bounds__(256, 1)
           const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
           mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
         }
+        if constexpr (SPLIT) {
+          const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
+                   kIdPV, 1u);
+        }
         mma_commit(bar(C::kBVE + st));
         mma_commit(bar(C::kBOR));
         return true;
@@ -213,6 +227,8 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t ph = (t / C::kStages) & 1;
         const int sb = t & 1;
         if (!mbar_wait(bar(C::kBKF + st), ph, abort_flag)) { ok = false; break; }
+        // SPLIT: P_lo of tile t - 2 lives in this S buffer until its P V is done
+        if (SPLIT && t >= 2 && !mbar_wait(bar(C::kBOR), (t - 2) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
         const uint32_t scol = tmem + (sb ? C::kColS1 : C::kColS0);
@@ -318,12 +334,21 @@ __global__ void __launch_bounds__(256, 1)
       }
       {
         const uint32_t pcol = tmem + lane_addr + (sb ? C::kColP1 : C::kColP0);
+        const uint32_t lcol = tmem + lane_addr + (sb ? C::kColS1 : C::kColS0) + 64;
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
           tmem_st_32x32b_x16(pcol + c0 / 2, pk);
+          if constexpr (SPLIT) {
+            uint32_t lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              lo[i] = pack2<BF16>(s[c0 + 2 * i] - unpack_lo<BF16>(pk[i]),
+                                  s[c0 + 2 * i + 1] - unpack_hi<BF16>(pk[i]));
+            tmem_st_32x32b_x16(lcol + c0 / 2, lo);
+          }
         }
       }
       tmem_wait_st();

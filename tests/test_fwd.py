@@ -177,3 +177,22 @@ def test_fwd_full_size_sampled(name):
                                   t.get("block_mask"))
     check(f"O[{b},{h}] whole head", o[b, h], o_ref[0, 0], TOL_O, t["q"].dtype)
     check(f"LSE[{b},{h}] whole head", lse[b, h], lse_ref[0, 0], TOL_LSE, torch.float32)
+
+
+@pytest.mark.parametrize("d,dt", [(128, "bf16"), (64, "f16")])
+def test_fwd_residual_path_is_accurate(d, dt):
+    """With o_res requested the forward feeds P to the tensor core as a
+    hi + lo pair: O itself still passes the output tolerance, and O + o_res
+    matches the exact O to a few 1e-4, far inside the rounding of O alone."""
+    import exact_io_aware_108_b300 as fa
+    t = inputs.make_qkv(2, 2, 512, d, dt, seed=21, qk_mult=2.0, with_dout=False)
+    q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse, o_res = fa.attention_forward(q, k, v, scale, causal=True, return_residual=True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+    o_ref, lse_ref = ref.attn_fwd(t["q"], t["k"], t["v"], scale, True)
+    check("O", o.cpu(), o_ref, TOL_O, q.dtype)
+    check("LSE", lse.cpu(), lse_ref, TOL_LSE, torch.float32)
+    o32 = o.cpu().double().numpy() + o_res.cpu().double().numpy()
+    assert np.max(np.abs(o32 - o_ref)) < 2e-3
