@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     fa_bwd_blocksparse,
     fa_bwd_finish,
     fa_bwd_main,
+    fa_bwd_noalloc,
+    fa_bwd_noalloc_max_workspace,
     fa_bwd_prepare,
     fa_bwd_workspace_size,
     fa_fwd,

@@ -19,7 +19,8 @@ FA_F16, FA_BF16 = 0, 1
 # every symbol include/fa.h declares
 EXPORTS = (
     "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_bwd_workspace_size", "fa_bwd",
-    "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish",
+    "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
+    "fa_bwd_noalloc_max_workspace",
     "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
 )
 
@@ -69,6 +70,10 @@ def load_library():
         lib.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd_main.argtypes = [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_finish.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_noalloc.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _vp]
+        lib.fa_bwd_noalloc.restype = _i
+        lib.fa_bwd_noalloc_max_workspace.argtypes = []
+        lib.fa_bwd_noalloc_max_workspace.restype = _sz
         lib.fa_get_device_error.argtypes = [_vp]
         lib.fa_status_str.argtypes = [_i]
         lib.fa_status_str.restype = ctypes.c_char_p
@@ -207,6 +212,23 @@ def fa_bwd_finish(dq, workspace, workspace_bytes=None, stream=None):
     _check(load_library().fa_bwd_finish(_ptr(dq), B, H, N, d, _dtype_code(dq), _ptr(workspace),
                                         _ws_bytes(workspace, workspace_bytes), _stream(stream)),
            "fa_bwd_finish")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale, causal=False, kv_len=None,
+                   block_mask=None, o_res=None, stream=None):
+    """fa_bwd without a workspace argument: the library's fixed scratch is used
+    (for callers that may not allocate device memory)."""
+    B, H, N, d = _dims(q)
+    _check(load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                         _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                         float(scale), int(bool(causal)), _dtype_code(q),
+                                         _ptr(kv_len), _ptr(block_mask), _ptr(o_res),
+                                         _stream(stream)),
+           "fa_bwd_noalloc")
+
+
+def fa_bwd_noalloc_max_workspace() -> int:
+    return int(load_library().fa_bwd_noalloc_max_workspace())
 
 
 def fa_get_device_error(stream=None) -> int:

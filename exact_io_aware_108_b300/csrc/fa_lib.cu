@@ -336,6 +336,34 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   return ok();
 }
 
+// ------------------------------------------------------------------------
+// Fixed scratch for fa_bwd_noalloc: callers that may not allocate device
+// memory get the backward's workspace from this array instead. It is part of
+// the library's device image, so every GPU that loads the library holds it
+// until the process exits. Every call shares it.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (host code may not use the symbol itself as a pointer).
+fa_status noalloc_scratch(void **out) {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  std::lock_guard<std::mutex> g(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,6 +433,29 @@ fa_status fa_bwd_finish(void *dq, int B, int H, int N, int d, fa_dtype dtype, vo
                   N, d, 1.0f, 0, dtype, nullptr, nullptr, false, nullptr, workspace,
                   workspace_bytes, stream, kFinish);
 }
+
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                         int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                         const int32_t *kv_len, const uint8_t *block_mask, const void *o_res,
+                         void *stream) {
+  Shape s;
+  fa_status r = check_common(B, H, N, d, scale, dtype, &s);
+  if (r != FA_OK) return r;
+  const size_t need = fa_bwd_ws_bytes(B, H, N, d);
+  if (need > kNoAllocScratchBytes)
+    return fail(FA_ERR_INVALID_ARG,
+                "fa_bwd_noalloc: these sizes need %zu bytes of scratch, more than the %zu bytes "
+                "built into the library; use fa_bwd with a caller-owned workspace",
+                need, kNoAllocScratchBytes);
+  void *ws = nullptr;
+  if ((r = noalloc_scratch(&ws)) != FA_OK) return r;
+  const bool sparse = block_mask != nullptr;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, sparse ? 0 : causal, dtype,
+                  kv_len, block_mask, sparse, o_res, ws, kNoAllocScratchBytes, stream);
+}
+
+size_t fa_bwd_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
 
 fa_status fa_get_device_error(void *stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -175,6 +175,44 @@ fa_status fa_bwd_finish(void *dq, int B, int H, int N, int d, fa_dtype dtype, vo
                         size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass for callers that cannot allocate device memory. (The paper
+ * has no counterpart: this is a library convenience.) Some callers may not
+ * call cudaMalloc or any allocator on the path that runs the backward: code
+ * that executes inside another framework's or engine's enqueue/execute
+ * callback, where device memory belongs to that host and allocating is
+ * forbidden or unsafe, and code bound to a fixed memory budget that cannot
+ * grow. They cannot supply fa_bwd's workspace, so this call uses a fixed
+ * scratch array built into the library instead; everything else (inputs and
+ * outputs) is still passed in, exactly as for fa_bwd / fa_bwd_blocksparse.
+ *   block_mask  NULL: dense or causal (as fa_bwd); non-NULL: block-sparse
+ *               (as fa_bwd_blocksparse; causal is ignored).
+ * Limits and behaviour:
+ *   - the scratch holds fa_bwd_noalloc_max_workspace() bytes (32 MiB); sizes
+ *     whose fa_bwd_workspace_size exceeds it are rejected with
+ *     FA_ERR_INVALID_ARG before anything runs (for d = 128 that is about
+ *     64K query rows: B * H * ceil(N / 128) * 128 <= 64527);
+ *   - the array is part of the library's device image: every GPU that loads
+ *     the library holds it until the process exits;
+ *   - the first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture;
+ *   - all calls share the one array and it keeps the last call's contents;
+ *     each call rewrites every part it reads (the dQ accumulator is zeroed
+ *     by the call itself), but two calls that overlap on the GPU (different
+ *     streams, or different host threads) race on it and must be ordered by
+ *     the caller;
+ *   - no cudaMalloc, cudaFree or other allocating routine is called.
+ */
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                         const int32_t *kv_len, const uint8_t *block_mask, const void *o_res,
+                         void *stream);
+
+/* Bytes of the scratch array fa_bwd_noalloc uses (its size limit). */
+size_t fa_bwd_noalloc_max_workspace(void);
+
+/*
  * Synchronises `stream`, then reads and clears the device error flag set by
  * a kernel whose pipeline wait timed out. Returns FA_OK, FA_ERR_TIMEOUT or
  * FA_ERR_CUDA (when the synchronisation itself failed).
