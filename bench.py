@@ -121,6 +121,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(flops_per_rank_step, ms_per_step_max, world):
+    """Weak scaling: every rank runs the same per-rank workload; the job's rate
+    is all ranks' flops divided by the slowest rank's time (TFLOP/s)."""
+    return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
+
+
+def rank_seed_offset(rank):
+    """Each rank draws its own independent problem (a different seed)."""
+    return int(rank)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 class Problem:
@@ -196,7 +219,7 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     fa.load_library()
     peaks = load_peaks()
-    probs = [Problem(inputs.WORKLOADS[n], rank, device) for n in SWEEP]
+    probs = [Problem(inputs.WORKLOADS[n], rank_seed_offset(rank), device) for n in SWEEP]
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
 
@@ -234,14 +257,10 @@ def run_ours(args, rank, world, local_rank):
         barrier()
     ms_total = t0.elapsed_time(t1)
     assert fa.fa_get_device_error(stream) == 0, "device error in the timed region"
-    ms_max = ms_total
-    if dist is not None:
-        tt = torch.tensor([ms_total], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms_total, dist, device)
     ms_step = ms_max / K
     flops_step = sum(p.flops_fwd + p.flops_bwd for p in probs)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_rate(flops_step, ms_step, world)
 
     # per-sweep-point breakdown and the dominant kernel (bwd_main) roofline
     sweep = []
@@ -288,12 +307,8 @@ def run_ours(args, rank, world, local_rank):
                 p.step_e2e(stream)
         e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_k
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_k, dist, device)
+    e2e = {"value": round(whole_job_rate(flops_step, e2e_ms, world), 1), "unit": "TFLOP/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes() for p in probs),
            "d2h_bytes_per_step": sum(p.d2h_bytes() for p in probs),
            "ms_per_step": round(e2e_ms, 3)}
