@@ -58,14 +58,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (one 128-byte-wide column block of a 128-row tile), 128-byte swizzle.
 // Rows past N read as zero.
 fa_status make_tile_map(CUtensorMap *m, const void *ptr, fa_dtype dt, int N, long long BH, int d,
-                        const char *name) {
+                        const char *name, unsigned box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, dt == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
