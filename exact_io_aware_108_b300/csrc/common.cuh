@@ -17,8 +17,9 @@ __device__ unsigned int g_fa_device_error = 0;
 // Slow path of a wait: poll until the phase completes, the CTA-wide abort
 // flag is raised by another role, or the time limit passes (then raise the
 // abort flag and the device error word). honor_abort = false is used when
-// draining copies in flight after an abort.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+// draining copies in flight after an abort. Inlined: a real call would be
+// shared by warpgroups that run under different setmaxnreg register limits.
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             volatile uint32_t *abort_flag, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {

@@ -15,6 +15,7 @@
 
 #include "fa.h"
 #include "fwd_kernel.cuh"
+#include "fwd2_kernel.cuh"
 #include "bwd_kernel.cuh"
 
 namespace {
@@ -137,10 +138,52 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   return FA_OK;
 }
 
+// Two-query-tile kernel; it relies on setmaxnreg shifting registers between
+// warpgroups, which is only safe when the kernel was built with exactly the
+// register count the split assumes (checked once per kernel and device).
+// Returns false (nothing launched) when that check fails.
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     const fa::FwdArgs &a, int nqb_grid, cudaStream_t st, fa_status *r) {
+  auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, SPLIT>;
+  static std::mutex mu;
+  static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (usable[dev] == 0) {
+      cudaFuncAttributes at;
+      usable[dev] = (cudaFuncGetAttributes(&at, reinterpret_cast<const void *>(kern)) == cudaSuccess &&
+                     at.numRegs == fa::Fwd2Cfg<D>::kLaunchRegs)
+                        ? 1
+                        : -1;
+    }
+    if (usable[dev] < 0) return false;
+  }
+  constexpr int smem = fa::Fwd2Cfg<D>::kSmemBytes;
+  cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) {
+    *r = cuda_fail(e, "cudaFuncSetAttribute(fwd2)");
+    return true;
+  }
+  kern<<<nqb_grid, 384, smem, st>>>(tq, tk, tv, a);
+  e = cudaGetLastError();
+  *r = (e != cudaSuccess) ? cuda_fail(e, "fwd2 launch") : FA_OK;
+  return true;
+}
+
 template <int D, bool BF16, bool SPLIT>
 fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
   if (sparse) return launch_fwd_t<D, BF16, false, true, SPLIT>(tq, tk, tv, a, grid, st);
+  // dense / causal / key padding: two query tiles per CTA
+  const long long bh = grid / a.nqt;
+  const int grid2 = static_cast<int>(bh * ((a.nqt + 1) / 2));
+  fa_status r = FA_OK;
+  if (causal ? try_launch_fwd2<D, BF16, true, SPLIT>(tq, tk, tv, a, grid2, st, &r)
+             : try_launch_fwd2<D, BF16, false, SPLIT>(tq, tk, tv, a, grid2, st, &r))
+    return r;
   if (causal) return launch_fwd_t<D, BF16, true, false, SPLIT>(tq, tk, tv, a, grid, st);
   return launch_fwd_t<D, BF16, false, false, SPLIT>(tq, tk, tv, a, grid, st);
 }

@@ -1,0 +1,350 @@
+// fwd2_kernel.cuh -- forward attention for sm_103a, two query tiles per CTA.
+//
+// The block loop of "Flash Attention: revolutionizing transformer
+// efficiency" (query blocks outer, key/value blocks inner, running max m and
+// sum l), as in fwd_kernel.cuh, but each CTA owns two 128-row query tiles A
+// and B of the same (batch, head) and one softmax warpgroup per tile. The MMA
+// thread alternates between the tiles -- S_A = Q_A K_j^T, S_B = Q_B K_j^T,
+// O_A += P_A V_j, O_B += P_B V_j -- so while one warpgroup runs its softmax
+// the tensor cores work on the other tile. K_j and V_j are loaded once for
+// both tiles.
+//
+// Roles (384 threads; setmaxnreg moves registers from warpgroup 0 to the two
+// softmax warpgroups):
+//   warp 0 lane 0  TMA producer (Q_A, Q_B once; K/V ring)
+//   warp 1         TMEM allocation; lane 0 issues every tcgen05.mma
+//   warps 4..7     softmax of tile A (thread r = query row r)
+//   warps 8..11    softmax of tile B
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B after it.
+// P (16-bit pairs) is written into the first 64 columns of its own, already
+// read S buffer; with SPLIT the low part of P goes into the other 64. QK^T of
+// the next key tile into that buffer waits for the P V that reads it.
+//
+// Online softmax: softmax_row (softmax_row.cuh), the same arithmetic as
+// fwd_kernel.cuh.
+#pragma once
+#include "common.cuh"
+#include "fwd_kernel.cuh"
+
+namespace fa {
+
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kKB = D / 64;
+  static constexpr int kQOff = 0;                          // Q_A, Q_B
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBQ = 0;
+  static constexpr int kBKF = 1;
+  static constexpr int kBVF = kBKF + kStages;
+  static constexpr int kBKE = kBVF + kStages;
+  static constexpr int kBVE = kBKE + kStages;
+  static constexpr int kBSF = kBVE + kStages;  // [2] S_X ready
+  static constexpr int kBPF = kBSF + 2;        // [2] P_X in TMEM (128 arrivals)
+  static constexpr int kBOR = kBPF + 2;        // [2] P_X V done
+  static constexpr int kBDR = kBOR + 2;
+  static constexpr int kNumBars = kBDR + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  __host__ __device__ static constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
+  static constexpr uint32_t kColO0 = 256;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColO0 + 2 * D <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // setmaxnreg split: launch with 168 registers x 384 threads; warpgroup 0
+  // gives back to 56, the two softmax warpgroups take 224 (sum unchanged).
+  static constexpr int kLaunchRegs = 168, kRegsLow = 56, kRegsHigh = 224;
+  static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kLaunchRegs * 384, "register split");
+};
+
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+__global__ void __launch_bounds__(384, 1)
+    fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using C = Fwd2Cfg<D>;
+  extern __shared__ uint8_t smem_raw2[];
+  const uint32_t raw = smem_u32(smem_raw2);
+  const uint32_t sbase = align_up_1024(raw);
+  uint8_t *smem = smem_raw2 + (sbase - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  volatile uint32_t *abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
+
+  // ---- work item: 256 query rows (tiles 2qb, 2qb+1) of one head
+  const int nqb = (a.nqt + 1) >> 1;
+  const int bh = blockIdx.x / nqb;
+  int qb = blockIdx.x % nqb;
+  if (CAUSAL) qb = nqb - 1 - qb;  // heaviest blocks first
+  const int b = bh / a.H;
+  int kvl = a.N;
+  if (a.kv_len != nullptr) {
+    const int v = a.kv_len[b];
+    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
+  }
+  const int nkt_eff = (kvl + 127) >> 7;
+  int n_tile[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int qt = 2 * qb + x;
+    n_tile[x] = (qt < a.nqt) ? (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff) : 0;
+  }
+  const int n_max = max(n_tile[0], n_tile[1]);
+  const bool has_b = (2 * qb + 1) < a.nqt;
+
+  if (tid == 0) {
+    mbar_init(bar(C::kBQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBKF + s), 1);
+      mbar_init(bar(C::kBVF + s), 1);
+      mbar_init(bar(C::kBKE + s), 1);
+      mbar_init(bar(C::kBVE + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::kBSF + x), 1);
+      mbar_init(bar(C::kBPF + x), 128);
+      mbar_init(bar(C::kBOR + x), 1);
+    }
+    mbar_init(bar(C::kBDR), 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_max > 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes * (has_b ? 2 : 1));
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kQOff + x * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQ),
+                           kb * 64, (2 * qb + x) * 128, bh, pol_q);
+      int nk = 0, nv = 0;
+      for (int t = 0; t < n_max; ++t) {
+        const int st = t % C::kStages;
+        const uint32_t ph = (t / C::kStages) & 1;
+        if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
+                           bar(C::kBKF + st), kb * 64, t * 128, bh, pol_kv);
+        nk = t + 1;
+        if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
+                           bar(C::kBVF + st), kb * 64, t * 128, bh, pol_kv);
+        nv = t + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(bar(C::kBQ), 0, abort_flag);
+        for (int t = max(0, nk - C::kStages); t < nk; ++t)
+          mbar_wait_drain(bar(C::kBKF + t % C::kStages), (t / C::kStages) & 1, abort_flag);
+        for (int t = max(0, nv - C::kStages); t < nv; ++t)
+          mbar_wait_drain(bar(C::kBVF + t % C::kStages), (t / C::kStages) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_f16(BF16, 128, D, false, true);
+      bool ok = mbar_wait(bar(C::kBQ), 0, abort_flag);
+      for (int t = 0; ok && t < n_max; ++t) {
+        const int st = t % C::kStages;
+        const uint32_t ph = (t / C::kStages) & 1;
+        if (!mbar_wait(bar(C::kBKF + st), ph, abort_flag)) { ok = false; break; }
+        const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (t >= n_tile[x]) continue;
+          // S_x still holds P_x of tile t - 1 until its P V is done
+          if (t >= 1 && !mbar_wait(bar(C::kBOR + x), (t - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qbase = sbase + C::kQOff + x * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
+                   sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBSF + x));
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBKE + st));
+        if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) { ok = false; break; }
+        const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (t >= n_tile[x]) continue;
+          if (!mbar_wait(bar(C::kBPF + x), t & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ocol = tmem + C::kColO0 + x * D;
+          const uint32_t pcol = tmem + C::col_s(x);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
+                   (t > 0 || ks > 0) ? 1u : 0u);
+          if constexpr (SPLIT) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
+          }
+          mma_commit(bar(C::kBOR + x));
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBVE + st));
+      }
+      mma_commit(bar(C::kBDR));
+      mbar_wait_drain(bar(C::kBDR), 0, abort_flag);
+    }
+  }
+    // teardown of warpgroup 0 (the two register regions do not rejoin)
+    tc_fence_before();
+    named_bar_sync(1, 384);
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, C::kTmemCols);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
+    // ------------------------------------------------------------ softmax of tile x
+    const int x = (warp - 4) >> 2;
+    const int row = (tid - 128) & 127;
+    const int qt = 2 * qb + x;
+    const int n = n_tile[x];
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t scol = tmem + lane_addr + C::col_s(x);
+    const uint32_t ocol = tmem + lane_addr + C::kColO0 + x * D;
+    const int q_row = qt * 128 + row;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      if (!mbar_wait_warp(bar(C::kBSF + x), t & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld_32x32b_x32(scol + 0, r0);
+        tmem_ld_32x32b_x32(scol + 32, r1);
+        tmem_ld_32x32b_x32(scol + 64, r2);
+        tmem_ld_32x32b_x32(scol + 96, r3);
+        tmem_wait_ld();
+        reg_fence_32(r0);
+        reg_fence_32(r1);
+        reg_fence_32(r2);
+        reg_fence_32(r3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(r0[c]);
+          s[32 + c] = __uint_as_float(r1[c]);
+          s[64 + c] = __uint_as_float(r2[c]);
+          s[96 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      int limit = kvl - t * 128;
+      if (CAUSAL && t == qt) limit = min(limit, row + 1);
+      float m_new, alpha;
+      const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      l = l * alpha + rs;
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t hi[16], lo[16];
+        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+        tmem_st_32x32b_x16(scol + c0 / 2, hi);
+        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
+      }
+      // rescale O_x (after the scores are dead, to keep registers low); O_x
+      // holds P_x V of tiles < t once that MMA is done
+      if (t > 0) {
+        if (!mbar_wait_warp(bar(C::kBOR + x), (t - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, m_new != m)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(ocol + c0, o);
+            tmem_wait_ld();
+            reg_fence_32(o);
+            scale32(o, alpha);
+            tmem_st_32x32b_x32(ocol + c0, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBPF + x));
+      m = m_new;
+    }
+    // ---- epilogue: O / l and LSE (rows of a missing tile B are skipped)
+    bool have_o = ok && n > 0;
+    if (have_o) {
+      have_o = mbar_wait_warp(bar(C::kBOR + x), (n - 1) & 1, abort_flag);
+      tc_fence_after();
+    }
+    if (qt < a.nqt) {
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      uint16_t *orow = static_cast<uint16_t *>(a.o) +
+                       (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (have_o) {
+          tmem_ld_32x32b_x32(ocol + c0, o);
+          tmem_wait_ld();
+          reg_fence_32(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t pk[16], rk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+          pk[i] = pack2<BF16>(x0, x1);
+          rk[i] = pack2<BF16>(x0 - unpack_lo<BF16>(pk[i]), x1 - unpack_hi<BF16>(pk[i]));
+        }
+        if (q_row < a.N) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          if (a.o_res != nullptr) {
+            uint4 *dr = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.o_res) +
+                                                  (orow - static_cast<uint16_t *>(a.o)) + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dr[v] = make_uint4(rk[4 * v], rk[4 * v + 1], rk[4 * v + 2], rk[4 * v + 3]);
+          }
+        }
+      }
+      if (q_row < a.N)
+        a.lse[static_cast<size_t>(bh) * a.N + q_row] =
+            (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    }
+    // teardown of the softmax warpgroups
+    tc_fence_before();
+    named_bar_sync(1, 384);
+  }
+}
+
+}  // namespace fa

@@ -23,13 +23,17 @@
 // Online softmax in base 2: x = s * scale * log2(e); p = 2^(x - m);
 // l <- 2^(m_old - m) l + sum p; O <- 2^(m_old - m) O + P V
 // (softmax decomposition and merger, section "The Math Behind Flash
-// Attention"). m is the exact running row max, so the largest probability of
-// a row is exactly 1 when it is rounded to 16 bits for the P V product; O is
-// rescaled in TMEM whenever any row of the warp sees a new max. (Letting m lag
-// the max, to skip rescales, rounds the dominant probability too: for sharp
-// bf16 softmax that doubled the error of O and of D = rowsum(dO * O).)
+// Attention"; the per-row update is softmax_row in softmax_row.cuh). Without
+// SPLIT m is the exact running row max, so the largest probability of a row
+// is exactly 1 when it is rounded to 16 bits for the P V product, and O is
+// rescaled in TMEM whenever any row of the warp sees a new max. (A lagging max
+// rounds the dominant probability too: for sharp bf16 softmax that doubled
+// the error of O and of D = rowsum(dO * O).) With SPLIT the P_lo product
+// recovers that rounding, so m may lag the max by up to a factor 2^8 and most
+// tiles need no rescale.
 #pragma once
 #include "common.cuh"
+#include "softmax_row.cuh"
 
 namespace fa {
 
@@ -285,36 +289,20 @@ __global__ void __launch_bounds__(256, 1)
       // mask: keys past kv_len / N, and keys after the query on the diagonal
       int limit = kvl - kt * 128;
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
-      if (limit < 128) {
+      float m_new, alpha;
+      const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      l = l * alpha + rs;
+      {
+        const uint32_t pcol = tmem + lane_addr + (sb ? C::kColP1 : C::kColP0);
+        const uint32_t lcol = tmem + lane_addr + (sb ? C::kColS1 : C::kColS0) + 64;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= limit) s[c] = -INFINITY;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t hi[16], lo[16];
+          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          tmem_st_32x32b_x16(pcol + c0 / 2, hi);
+          if constexpr (SPLIT) tmem_st_32x32b_x16(lcol + c0 / 2, lo);
+        }
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
-      }
-      const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = fmaxf(m, mxs);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);
-      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
-        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
-        s[c + 2] = ex2_approx(fmaf(s[c + 2], sl2, -m_use));
-        s[c + 3] = ex2_approx(fmaf(s[c + 3], sl2, -m_use));
-        rs0 += s[c];
-        rs1 += s[c + 1];
-        rs2 += s[c + 2];
-        rs3 += s[c + 3];
-      }
-      l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
       if (t > 0) {
         // O holds P_{t-1} V_{t-1} only once that MMA is done
         if (!mbar_wait_warp(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
@@ -326,28 +314,8 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c0, o);
             tmem_wait_ld();
             reg_fence_32(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            scale32(o, alpha);
             tmem_st_32x32b_x32(tmem + lane_addr + C::kColO + c0, o);
-          }
-        }
-      }
-      {
-        const uint32_t pcol = tmem + lane_addr + (sb ? C::kColP1 : C::kColP0);
-        const uint32_t lcol = tmem + lane_addr + (sb ? C::kColS1 : C::kColS0) + 64;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
-          tmem_st_32x32b_x16(pcol + c0 / 2, pk);
-          if constexpr (SPLIT) {
-            uint32_t lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              lo[i] = pack2<BF16>(s[c0 + 2 * i] - unpack_lo<BF16>(pk[i]),
-                                  s[c0 + 2 * i + 1] - unpack_hi<BF16>(pk[i]));
-            tmem_st_32x32b_x16(lcol + c0 / 2, lo);
           }
         }
       }

@@ -1,0 +1,85 @@
+// softmax_row.cuh -- the online-softmax update of one query row over one
+// 128-key tile, shared by the forward kernels so that every forward path
+// performs exactly the same arithmetic (dense and block-sparse results are
+// then bitwise comparable).
+//
+// In base 2 ("Flash Attention: revolutionizing transformer efficiency",
+// section "The Math Behind Flash Attention": softmax decomposition and
+// merger): x_c = s_c * scale * log2(e); the running max m moves to
+// max(m, max_c x_c) (LAZY: only when that exceeds m by more than 8, i.e. a
+// factor 256); p_c = 2^(x_c - m_new); alpha = 2^(m_old - m_new); the caller
+// updates l <- alpha l + sum_c p_c and O <- alpha O + P V.
+#pragma once
+#include "ptx.cuh"
+
+namespace fa {
+
+// s: the 128 raw scores of this row (entries c >= limit are masked);
+// on return s holds p (fp32). Returns the tile's sum of p.
+template <bool LAZY>
+__device__ __forceinline__ float softmax_row(float (&s)[128], int limit, float sl2, float m,
+                                             float &m_new, float &alpha) {
+  if (limit < 128) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= limit) s[c] = -INFINITY;
+  }
+  float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+  float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+  for (int c = 12; c < 124; c += 8) {
+    mx0 = fmax3(mx0, s[c], s[c + 1]);
+    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+  }
+  mx0 = fmax3(mx0, s[124], s[125]);
+  mx1 = fmax3(mx1, s[126], s[127]);
+  const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+  m_new = LAZY ? ((mxs > m + 8.0f) ? mxs : m) : fmaxf(m, mxs);
+  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+  alpha = ex2_approx(m - m_use);
+  const float nm = -m_use;
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 128; c += 4) {
+    ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, sl2, nm, nm);
+    ffma2(s[c + 2], s[c + 3], s[c + 2], s[c + 3], sl2, sl2, nm, nm);
+    s[c] = ex2_approx(s[c]);
+    s[c + 1] = ex2_approx(s[c + 1]);
+    s[c + 2] = ex2_approx(s[c + 2]);
+    s[c + 3] = ex2_approx(s[c + 3]);
+    fadd2(a0, a1, a0, a1, s[c], s[c + 1]);
+    fadd2(b0, b1, b0, b1, s[c + 2], s[c + 3]);
+  }
+  return (a0 + a1) + (b0 + b1);
+}
+
+// Packs p (fp32) of columns c0 .. c0+31 into 16 16-bit pairs (hi) and, for
+// the split product, the rounding remainders (lo).
+template <bool BF16, bool SPLIT>
+__device__ __forceinline__ void pack_p32(const float (&s)[128], int c0, uint32_t (&hi)[16],
+                                         uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    hi[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
+    if constexpr (SPLIT) {
+      float r0, r1;
+      fsub2(r0, r1, s[c0 + 2 * i], s[c0 + 2 * i + 1], unpack_lo<BF16>(hi[i]), unpack_hi<BF16>(hi[i]));
+      lo[i] = pack2<BF16>(r0, r1);
+    }
+  }
+}
+
+// O row chunk (32 fp32 values) *= alpha.
+__device__ __forceinline__ void scale32(uint32_t (&o)[32], float alpha) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float x0, x1;
+    fmul2(x0, x1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+    o[i] = __float_as_uint(x0);
+    o[i + 1] = __float_as_uint(x1);
+  }
+}
+
+}  // namespace fa
