@@ -9,8 +9,9 @@
 //   dK_j += scale dS^T Q_i      dQ_i += scale dS K_j
 //
 // Three kernels:
-//   bwd_pre_kernel   D_i and LSE_i * log2(e) per query row (padded to whole
-//                    128-row tiles; pad rows get D = 0, LSE = +inf so P = 0)
+//   bwd_pre_kernel   -scale * D_i and -LSE_i * log2(e) per query row (padded
+//                    to whole 128-row tiles; pad rows get D = 0, LSE = +inf so
+//                    P = 0)
 //                    and zeroes the fp32 dQ accumulator. D_i = dO_i . O_i
 //                    uses O plus its rounding residual when the forward
 //                    wrote one: with bf16 O alone the rounding of O moves
@@ -44,8 +45,8 @@ struct BwdArgs {
   const void *o, *dout;
   const void *o_res;  // rounding residual of O (same 16-bit type) or null
   const float *lse;
-  float *lse_l2;    // [BH, nqt*128]
-  float *delta;     // [BH, nqt*128]
+  float *lse_l2;    // [BH, nqt*128]  -LSE * log2(e)
+  float *delta;     // [BH, nqt*128]  -scale * D
   float *dq_acc;    // [BH, nqt*128, D]
   const int32_t *kv_len;
   const uint8_t *block_mask;
@@ -110,13 +111,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
 #pragma unroll
     for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (live && sub == 0) {
-      a.delta[row] = acc;
-      float l2 = INFINITY;
+      // stored negated (and D pre-scaled) so the main kernel forms
+      // P = 2^(s * scale * log2 e + nl) and dS = P * (dP * scale + nd)
+      // with one packed FMA per pair
+      a.delta[row] = -a.scale * acc;
+      float nl = -INFINITY;
       if (i < a.N) {
         const float l = a.lse[static_cast<size_t>(bh) * a.N + i];
-        if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+        if (l != -INFINITY) nl = -l * 1.4426950408889634f;
       }
-      a.lse_l2[row] = l2;
+      a.lse_l2[row] = nl;
     }
   }
 }
@@ -363,30 +367,43 @@ __global__ void __launch_bounds__(384, 1)
     int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
     for (int u = 0; u < n_iter; ++u) {
       const int st = u & 1;
-      const float *lse_s = reinterpret_cast<const float *>(smem + C::kLseOff + st * 512);
-      const float *dl_s = reinterpret_cast<const float *>(smem + C::kDeltaOff + st * 512);
+      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + C::kLseOff + st * 512);
+      const float4 *nd4 = reinterpret_cast<const float4 *>(smem + C::kDeltaOff + st * 512);
       if (!mbar_wait_warp(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(bar(C::kBSF), u & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      // causal: query c of this tile sees key r iff qi*128 + c >= key
-      const int cmin = CAUSAL ? (key - qi * 128) : -1;
+      // causal: query c of this tile sees key r iff qi*128 + c >= key; a dead
+      // key row sees nothing
+      const int cmin = !key_live ? 128 : (CAUSAL ? (key - qi * 128) : -1);
       // Two halves of 64 queries: P (fp32, kept in registers for dS) ->
       // P^T (16-bit) into TMEM columns [32h, 32h+32) of the S^T region (the
       // scores there were already read), then dS^T of the same queries.
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float p[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t sr[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h + c0, sr);
+        {
+          uint32_t s0[32], s1[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h, s0);
+          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h + 32, s1);
           tmem_wait_ld();
-          reg_fence_32(sr);
+          reg_fence_32(s0);
+          reg_fence_32(s1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 64 * h + c0 + i;
-            const float x = ex2_approx(fmaf(__uint_as_float(sr[i]), sl2, -lse_s[c]));
-            p[c0 + i] = (!key_live || c < cmin) ? 0.f : x;
+          for (int i = 0; i < 64; i += 4) {
+            const float4 nl = nl4[(64 * h + i) >> 2];
+            const uint32_t *src = i < 32 ? &s0[i] : &s1[i - 32];
+            ffma2(p[i], p[i + 1], __uint_as_float(src[0]), __uint_as_float(src[1]), sl2, sl2, nl.x, nl.y);
+            ffma2(p[i + 2], p[i + 3], __uint_as_float(src[2]), __uint_as_float(src[3]), sl2, sl2, nl.z,
+                  nl.w);
+            p[i] = ex2_approx(p[i]);
+            p[i + 1] = ex2_approx(p[i + 1]);
+            p[i + 2] = ex2_approx(p[i + 2]);
+            p[i + 3] = ex2_approx(p[i + 3]);
+          }
+          if (cmin > 64 * h) {  // some columns of this half are masked for this key
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (64 * h + i < cmin) p[i] = 0.f;
           }
         }
 #pragma unroll
@@ -405,19 +422,27 @@ __global__ void __launch_bounds__(384, 1)
           if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
         }
+        uint32_t d0[32], d1[32];
+        tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h, d0);
+        tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h + 32, d1);
+        tmem_wait_ld();
+        reg_fence_32(d0);
+        reg_fence_32(d1);
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t dr[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h + c0, dr);
-          tmem_wait_ld();
-          reg_fence_32(dr);
+          const uint32_t *dr = c0 == 0 ? d0 : d1;
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int c = 64 * h + c0 + i;
-            const float ds0 = scale * p[c0 + i] * (__uint_as_float(dr[i]) - dl_s[c]);
-            const float ds1 = scale * p[c0 + i + 1] * (__uint_as_float(dr[i + 1]) - dl_s[c + 1]);
-            w[i / 2] = pack2<BF16>(ds0, ds1);
+          for (int i = 0; i < 32; i += 4) {
+            // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
+            const float4 nd = nd4[(64 * h + c0 + i) >> 2];
+            float t0, t1, t2, t3;
+            ffma2(t0, t1, __uint_as_float(dr[i]), __uint_as_float(dr[i + 1]), scale, scale, nd.x, nd.y);
+            ffma2(t2, t3, __uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3]), scale, scale, nd.z, nd.w);
+            fmul2(t0, t1, t0, t1, p[c0 + i], p[c0 + i + 1]);
+            fmul2(t2, t3, t2, t3, p[c0 + i + 2], p[c0 + i + 3]);
+            w[i / 2] = pack2<BF16>(t0, t1);
+            w[i / 2 + 1] = pack2<BF16>(t2, t3);
           }
           // row r of the dS^T tile, queries 64h+c0 .. +31 = 4 16-byte chunks of
           // the 128-byte row in region h, swizzled by (r & 7)
