@@ -504,35 +504,35 @@ __global__ void __launch_bounds__(384, 1)
     for (int u = 0; u < n_iter; ++u) {
       if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
       tc_fence_after();
+      // read the whole partial into registers, release the TMEM buffer (the
+      // next dP^T MMA may overwrite it), then reduce into the accumulator
+      uint32_t v[4][32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j * 32 < (C::kDqT ? 128 : D)) tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + j * 32, v[j]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j * 32 < (C::kDqT ? 128 : D)) reg_fence_32(v[j]);
+      tc_fence_before();
+      mbar_arrive(bar(C::kBDQE));
       if constexpr (C::kDqT) {
         // thread r holds channel r of the 128 queries of this tile
         float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128) * D + r;
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + c0, v);
-          tmem_wait_ld();
-          reg_fence_32(v);
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) atomicAdd(acc + (c0 + i) * D, __uint_as_float(v[i]));
-        }
+          for (int i = 0; i < 32; ++i) atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]));
       } else {
         float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + c0, v);
-          tmem_wait_ld();
-          reg_fence_32(v);
+        for (int j = 0; j < D / 32; ++j)
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            atomicAdd(reinterpret_cast<float4 *>(acc + c0 + i),
-                      make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
-        }
+            atomicAdd(reinterpret_cast<float4 *>(acc + j * 32 + i),
+                      make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
+                                  __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBDQE));
       qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
     }
   }
