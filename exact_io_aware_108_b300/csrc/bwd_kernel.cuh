@@ -23,18 +23,30 @@
 //                    so P^T and dS^T are row-local to one thread per key.
 //   bwd_dq_kernel    dQ accumulator (fp32) -> dQ (fp16/bf16).
 //
-// Main-kernel roles (384 threads):
+// Main-kernel roles (512 threads; setmaxnreg moves registers from
+// warpgroup 0 to the other three):
 //   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
 //                   query tile i through a two-stage ring.
 //   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
-//   warps 4..7      thread r owns key r: P^T row -> TMEM (16-bit), dS^T row
-//                   -> shared memory (16-bit, scale folded in, computed from
-//                   the fp32 P); final dK, dV.
-//   warps 8..11     read the dQ partial from TMEM and add it to the fp32
+//   warpgroups 1, 2 thread r owns key r for one 64-query half h of the tile:
+//                   P^T row -> TMEM (16-bit), dS^T row -> shared memory
+//                   (16-bit, scale folded in, computed from the fp32 P); at
+//                   the end warpgroup 1 writes dK, warpgroup 2 writes dV.
+//                   Each thread reads S^T and dP^T once per tile (one TMEM
+//                   round trip each), and the two warpgroups share each SM
+//                   sub-partition so one hides the other's TMEM latency.
+//   warpgroup 3     reads the dQ partial from TMEM and adds it to the fp32
 //                   accumulator (d = 128: thread r owns head-dim channel r of
 //                   the transposed partial; d = 64: thread r owns query r).
-// TMEM columns: dK [0,D), dV [D,2D), S^T [2D,2D+128) (P^T aliases its first
-// 64 columns), dP^T [2D+128, 2D+256) (the dQ partial reuses it once dS is out).
+// The MMA issue order per query tile i is dP_i, dV_i, dQ_i, S_{i+1}, dK_i
+// for d = 128: the next score tile is computed before dK_i, so the P phase
+// of tile i+1 overlaps the dK_i product and the dQ_i read-out, while the Q
+// stage of tile i+1 still has most of a tile's time to land (its load
+// latency grows to several thousand cycles under the dQ reduction traffic).
+// For d = 64 (smaller tiles, shorter loads) S_{i+1} goes right after dV_i.
+// TMEM columns: dK [0,D), dV [D,2D), S^T [2D,2D+128) (half h's P^T aliases
+// columns [64h, 64h+32) of it), dP^T [2D+128, 2D+256); the dQ partial reuses
+// the dP^T columns for d = 128 and has its own 64 columns for d = 64.
 #pragma once
 #include "common.cuh"
 
@@ -167,9 +179,18 @@ struct BwdCfg {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  static constexpr uint32_t kColDQ = kDqT ? kColDP : 2 * D + 256;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColDP + 128 <= kTmemCols, "TMEM budget");
+  // MMA order: S_{i+1} right after dV_i (d = 64) or after dQ_i (d = 128,
+  // where the Q load of tile i+1 needs the longer window); both measured.
+  static constexpr bool kSAfterDV = (D == 64);
+  static_assert(kColDP + 128 <= kTmemCols && kColDQ + (kDqT ? 128 : D) <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // setmaxnreg split: launch with 128 registers x 512 threads; warpgroup 0
+  // (producer, MMA issuer) gives registers to the three compute warpgroups.
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128, kRegsLow = 56, kRegsHigh = 152;
+  static_assert(kRegsLow * 128 + kRegsHigh * 384 <= kLaunchRegs * kThreads, "register split");
 };
 
 // Next kept query tile >= from for key tile kt (block-sparse column scan).
@@ -180,7 +201,7 @@ __device__ __forceinline__ int next_kept(const uint8_t *mask, int nkt, int nqt, 
 }
 
 template <int D, bool BF16, bool CAUSAL, bool SPARSE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdArgs a) {
@@ -221,13 +242,12 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBQF + s), 1);
       mbar_init(bar(C::kBQE + s), 1);
+      mbar_init(bar(C::kBPR + s), 128);
     }
     mbar_init(bar(C::kBSF), 1);
     mbar_init(bar(C::kBDPF), 1);
-    mbar_init(bar(C::kBPR), 128);
-    mbar_init(bar(C::kBPR + 1), 128);
     mbar_init(bar(C::kBDV), 1);
-    mbar_init(bar(C::kBDSR), 128);
+    mbar_init(bar(C::kBDSR), 256);
     mbar_init(bar(C::kBDQF), 1);
     mbar_init(bar(C::kBDQE), 128);
     mbar_init(bar(C::kBFIN), 1);
@@ -249,6 +269,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = misc[0];
   const long long tile_rows = static_cast<long long>(a.nqt) * 128;
 
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_iter > 0) {
@@ -290,25 +312,31 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t kIdKV = idesc_f16(BF16, 128, D, false, true);      // dK, dV
       constexpr uint32_t kIdQ = C::kDqT ? idesc_f16(BF16, 128, 128, true, true)  // dQ^T
                                         : idesc_f16(BF16, 128, D, true, true);   // dQ
-      const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sDS = sbase + C::kdSOff;
-      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag);
-      for (int u = 0; ok && u < n_iter; ++u) {
-        const int st = u & 1;
-        const uint32_t sQ = sbase + C::kQOff + st * C::kTileBytes;
-        const uint32_t sdO = sbase + C::kdOOff + st * C::kTileBytes;
-        if (!mbar_wait(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
-        // S^T region is free once the previous dV MMA has read P^T from it
-        if (u > 0 && !mbar_wait(bar(C::kBDV), (u - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      // S^T = K_j Q_i^T for the query tile in stage st
+      auto issue_s = [&](int st) {
+        const uint32_t sb = opaque_u32(sbase);
+        const uint32_t sK = sb + C::kKOff, sQ = sb + C::kQOff + st * C::kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // S^T = K_j Q_i^T
+        for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
           mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
                  kIdSS, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF));
-        // dP^T region is free once the previous dQ partial has been read out
-        if (u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
+      };
+      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int u = 0; ok && u < n_iter; ++u) {
+        const int st = u & 1;
+        const uint32_t sb = opaque_u32(sbase);
+        const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff, sDS = sb + C::kdSOff;
+        const uint32_t sQ = sb + C::kQOff + st * C::kTileBytes;
+        const uint32_t sdO = sb + C::kdOOff + st * C::kTileBytes;
+        // d = 128: the dP^T columns hold the previous dQ partial until read out
+        if (C::kDqT && u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
@@ -323,27 +351,45 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + (4 * h + ks) * 8,
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks,
                    sdesc_sw128(sdO + (4 * h + ks) * 2048, 16384, 1024), kIdKV,
                    (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(bar(C::kBDV));
+        if (C::kSAfterDV && u + 1 < n_iter) {
+          // next score tile: its Q stage must have landed, and the S^T
+          // columns are free once this tile's dV products have read P^T
+          if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((u + 1) >> 1) & 1, abort_flag) ||
+              !mbar_wait(bar(C::kBDV), u & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(st ^ 1);
+        }
         if (!mbar_wait(bar(C::kBDSR), u & 1, abort_flag)) { ok = false; break; }
+        // d = 64: the dQ columns hold the previous partial until read out
+        if (!C::kDqT && u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // dQ first, so its read-out overlaps the dK MMA
+        // dQ first, so its read-out overlaps the next S^T and the dK MMA
         if constexpr (C::kDqT) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
-            mma_ss(tmem + C::kColDP, sdesc_sw128(sK + ks * 2048, 16384, 1024),
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + ks * 2048, 16384, 1024),
                    sdesc_sw128(sDS + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
         } else {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dQ_i = dS K_j (dS read MN-major from the dS^T buffer)
-            mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
                    sdesc_sw128(sK + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBDQF));
+        if (!C::kSAfterDV && u + 1 < n_iter) {
+          // next score tile: its Q stage must have landed, and the S^T
+          // columns are free once this tile's dV products have read P^T
+          if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((u + 1) >> 1) & 1, abort_flag) ||
+              !mbar_wait(bar(C::kBDV), u & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(st ^ 1);
+        }
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
           mma_ss(tmem + C::kColDK,
@@ -355,165 +401,171 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(bar(C::kBFIN));
       mbar_wait_drain(bar(C::kBFIN), 0, abort_flag);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ P^T and dS^T
-    const int r = tid - 128;  // key row within the tile
+  }
+    // teardown of warpgroup 0 (the two register regions do not rejoin)
+    tc_fence_before();
+    named_bar_sync(1, C::kThreads);
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, C::kTmemCols);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (warp < 12) {
+    // ------------------------------------------------------------ P^T and dS^T, one query half
+    const int h = (warp >> 2) - 1;  // query half: columns [64h, 64h+64) of the tile
+    const int r = tid & 127;         // key row within the tile
     const int key = kt * 128 + r;
     const bool key_live = key < kvl;
     const float sl2 = a.scale_log2, scale = a.scale;
-    const uint32_t sDS = sbase + C::kdSOff;
+    const uint32_t sDS = sbase + C::kdSOff + h * 16384;
+    const uint32_t col_s = tmem + lane_addr + C::kColS + 64 * h;
+    const uint32_t col_dp = tmem + lane_addr + C::kColDP + 64 * h;
     bool ok = true;
     int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
     for (int u = 0; u < n_iter; ++u) {
       const int st = u & 1;
-      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + C::kLseOff + st * 512);
-      const float4 *nd4 = reinterpret_cast<const float4 *>(smem + C::kDeltaOff + st * 512);
+      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + C::kLseOff + st * 512 + h * 256);
+      const float4 *nd4 = reinterpret_cast<const float4 *>(smem + C::kDeltaOff + st * 512 + h * 256);
       if (!mbar_wait_warp(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(bar(C::kBSF), u & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       // causal: query c of this tile sees key r iff qi*128 + c >= key; a dead
-      // key row sees nothing
-      const int cmin = !key_live ? 128 : (CAUSAL ? (key - qi * 128) : -1);
-      // Two halves of 64 queries: P (fp32, kept in registers for dS) ->
-      // P^T (16-bit) into TMEM columns [32h, 32h+32) of the S^T region (the
-      // scores there were already read), then dS^T of the same queries.
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float p[64];
-        {
-          uint32_t s0[32], s1[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h, s0);
-          tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + 64 * h + 32, s1);
-          tmem_wait_ld();
-          reg_fence_32(s0);
-          reg_fence_32(s1);
-#pragma unroll
-          for (int i = 0; i < 64; i += 4) {
-            const float4 nl = nl4[(64 * h + i) >> 2];
-            const uint32_t *src = i < 32 ? &s0[i] : &s1[i - 32];
-            ffma2(p[i], p[i + 1], __uint_as_float(src[0]), __uint_as_float(src[1]), sl2, sl2, nl.x, nl.y);
-            ffma2(p[i + 2], p[i + 3], __uint_as_float(src[2]), __uint_as_float(src[3]), sl2, sl2, nl.z,
-                  nl.w);
-            p[i] = ex2_approx(p[i]);
-            p[i + 1] = ex2_approx(p[i + 1]);
-            p[i + 2] = ex2_approx(p[i + 2]);
-            p[i + 3] = ex2_approx(p[i + 3]);
-          }
-          if (cmin > 64 * h) {  // some columns of this half are masked for this key
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (64 * h + i < cmin) p[i] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack2<BF16>(p[2 * (c0 + i)], p[2 * (c0 + i) + 1]);
-          tmem_st_32x32b_x16(tmem + lane_addr + C::kColS + 32 * h + c0, w);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(C::kBPR + h));
-        if (h == 0) {
-          if (!mbar_wait_warp(bar(C::kBDPF), u & 1, abort_flag)) { ok = false; break; }
-          // the previous dQ/dK MMAs must be done reading dS before it is rewritten
-          if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
-        uint32_t d0[32], d1[32];
-        tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h, d0);
-        tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + 64 * h + 32, d1);
+      // key row sees nothing. Local column i is query 64h + i.
+      const int cmin = (!key_live ? 128 : (CAUSAL ? (key - qi * 128) : -1)) - 64 * h;
+      // P (fp32, kept in registers for dS) -> P^T (16-bit) into the first
+      // 32 columns of this half's S^T columns (already read), then dS^T.
+      float p[64];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld_32x32b_x32(col_s, s0);
+        tmem_ld_32x32b_x32(col_s + 32, s1);
         tmem_wait_ld();
-        reg_fence_32(d0);
-        reg_fence_32(d1);
+        reg_fence_32(s0);
+        reg_fence_32(s1);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          const uint32_t *dr = c0 == 0 ? d0 : d1;
-          uint32_t w[16];
+        for (int i = 0; i < 64; i += 4) {
+          const float4 nl = nl4[i >> 2];
+          const uint32_t *src = i < 32 ? &s0[i] : &s1[i - 32];
+          ffma2(p[i], p[i + 1], __uint_as_float(src[0]), __uint_as_float(src[1]), sl2, sl2, nl.x, nl.y);
+          ffma2(p[i + 2], p[i + 3], __uint_as_float(src[2]), __uint_as_float(src[3]), sl2, sl2, nl.z,
+                nl.w);
+          p[i] = ex2_approx(p[i]);
+          p[i + 1] = ex2_approx(p[i + 1]);
+          p[i + 2] = ex2_approx(p[i + 2]);
+          p[i + 3] = ex2_approx(p[i + 3]);
+        }
+        if (cmin > 0) {  // some columns of this half are masked for this key
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
-            const float4 nd = nd4[(64 * h + c0 + i) >> 2];
-            float t0, t1, t2, t3;
-            ffma2(t0, t1, __uint_as_float(dr[i]), __uint_as_float(dr[i + 1]), scale, scale, nd.x, nd.y);
-            ffma2(t2, t3, __uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3]), scale, scale, nd.z, nd.w);
-            fmul2(t0, t1, t0, t1, p[c0 + i], p[c0 + i + 1]);
-            fmul2(t2, t3, t2, t3, p[c0 + i + 2], p[c0 + i + 3]);
-            w[i / 2] = pack2<BF16>(t0, t1);
-            w[i / 2 + 1] = pack2<BF16>(t2, t3);
-          }
-          // row r of the dS^T tile, queries 64h+c0 .. +31 = 4 16-byte chunks of
-          // the 128-byte row in region h, swizzled by (r & 7)
-          const uint32_t rowb = sDS + h * 16384 + r * 128;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint32_t chunk = ((c0 >> 3) + v) ^ (r & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + chunk * 16),
-                         "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3])
-                         : "memory");
-          }
+          for (int i = 0; i < 64; ++i)
+            if (i < cmin) p[i] = 0.f;
         }
       }
-      if (!ok) break;
+#pragma unroll
+      for (int c0 = 0; c0 < 32; c0 += 16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack2<BF16>(p[2 * (c0 + i)], p[2 * (c0 + i) + 1]);
+        tmem_st_32x32b_x16(col_s + c0, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBPR + h));
+      if (!mbar_wait_warp(bar(C::kBDPF), u & 1, abort_flag)) { ok = false; break; }
+      // the previous dQ/dK MMAs must be done reading dS before it is rewritten
+      if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t d0[32], d1[32];
+      tmem_ld_32x32b_x32(col_dp, d0);
+      tmem_ld_32x32b_x32(col_dp + 32, d1);
+      tmem_wait_ld();
+      reg_fence_32(d0);
+      reg_fence_32(d1);
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        const uint32_t *dr = c0 == 0 ? d0 : d1;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
+          const float4 nd = nd4[(c0 + i) >> 2];
+          float t0, t1, t2, t3;
+          ffma2(t0, t1, __uint_as_float(dr[i]), __uint_as_float(dr[i + 1]), scale, scale, nd.x, nd.y);
+          ffma2(t2, t3, __uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3]), scale, scale, nd.z, nd.w);
+          fmul2(t0, t1, t0, t1, p[c0 + i], p[c0 + i + 1]);
+          fmul2(t2, t3, t2, t3, p[c0 + i + 2], p[c0 + i + 3]);
+          w[i / 2] = pack2<BF16>(t0, t1);
+          w[i / 2 + 1] = pack2<BF16>(t2, t3);
+        }
+        // row r of the dS^T tile, queries 64h+c0 .. +31 = 4 16-byte chunks of
+        // the 128-byte row in region h, swizzled by (r & 7)
+        const uint32_t rowb = sDS + r * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t chunk = ((c0 >> 3) + v) ^ (r & 7);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + chunk * 16),
+                       "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3])
+                       : "memory");
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kBDSR));
       qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
     }
-    // ---- dK, dV epilogue
+    // ---- epilogue: warpgroup 1 writes dK, warpgroup 2 writes dV
     bool have = ok && n_iter > 0;
     if (have) {
       have = mbar_wait_warp(bar(C::kBFIN), 0, abort_flag);
       tc_fence_after();
     }
-    const size_t orow = (static_cast<size_t>(bh) * a.N + static_cast<size_t>(key)) * D;
+    uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
+                    (static_cast<size_t>(bh) * a.N + static_cast<size_t>(key)) * D;
+    uint32_t v[D / 32][32];
+    if (have) {
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      uint16_t *dst = static_cast<uint16_t *>(which == 0 ? a.dk : a.dv) + orow;
-      const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
+      for (int j = 0; j < D / 32; ++j)
+        tmem_ld_32x32b_x32(tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV) + 32 * j, v[j]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        if (have) {
-          tmem_ld_32x32b_x32(tmem + lane_addr + col + c0, v);
-          tmem_wait_ld();
-          reg_fence_32(v);
-        } else {
+      for (int j = 0; j < D / 32; ++j) reg_fence_32(v[j]);
+    } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        uint32_t pk[16];
+      for (int j = 0; j < D / 32; ++j)
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        if (key < a.N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+        for (int i = 0; i < 32; ++i) v[j][i] = 0u;
+    }
+    if (key < a.N) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
+      for (int j = 0; j < D / 32; ++j) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack2<BF16>(__uint_as_float(v[j][8 * q]), __uint_as_float(v[j][8 * q + 1])),
+                             pack2<BF16>(__uint_as_float(v[j][8 * q + 2]), __uint_as_float(v[j][8 * q + 3])),
+                             pack2<BF16>(__uint_as_float(v[j][8 * q + 4]), __uint_as_float(v[j][8 * q + 5])),
+                             pack2<BF16>(__uint_as_float(v[j][8 * q + 6]), __uint_as_float(v[j][8 * q + 7])));
       }
     }
-  } else if (warp >= 8) {
+    } else {
     // ------------------------------------------------------------ dQ partials
-    const int r = tid - 256;  // query row within the tile
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = tid & 127;  // d = 128: head-dim channel; d = 64: query row
     int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
     for (int u = 0; u < n_iter; ++u) {
       if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
       tc_fence_after();
-      // read the whole partial into registers, release the TMEM buffer (the
-      // next dP^T MMA may overwrite it), then reduce into the accumulator
-      uint32_t v[4][32];
+      // read the whole partial into registers, release the TMEM columns
+      // (the next dP^T or dQ MMA may overwrite them), then reduce into the
+      // accumulator
+      constexpr int kCols = C::kDqT ? 128 : D;
+      uint32_t v[kCols / 32][32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j * 32 < (C::kDqT ? 128 : D)) tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDP + j * 32, v[j]);
+      for (int j = 0; j < kCols / 32; ++j) tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDQ + j * 32, v[j]);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j * 32 < (C::kDqT ? 128 : D)) reg_fence_32(v[j]);
+      for (int j = 0; j < kCols / 32; ++j) reg_fence_32(v[j]);
       tc_fence_before();
       mbar_arrive(bar(C::kBDQE));
       if constexpr (C::kDqT) {
@@ -535,14 +587,10 @@ __global__ void __launch_bounds__(384, 1)
       }
       qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    }
+    // teardown of the compute warpgroups
+    tc_fence_before();
+    named_bar_sync(1, C::kThreads);
   }
 }
 

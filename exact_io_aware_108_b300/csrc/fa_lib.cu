@@ -259,9 +259,28 @@ fa_status launch_bwd_main_t(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             const CUtensorMap &tdo, const fa::BwdArgs &a, int grid, cudaStream_t st) {
   auto kern = fa::bwd_main_kernel<D, BF16, CAUSAL, SPARSE>;
   constexpr int smem = fa::BwdCfg<D>::kSmemBytes;
+  // The kernel moves registers between warpgroups with setmaxnreg; the split
+  // only fits when it was built with exactly the register count it assumes.
+  static std::mutex mu;
+  static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(FA_ERR_CUDA, "bwd: cannot query the current device");
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (usable[dev] == 0) {
+      cudaFuncAttributes at;
+      usable[dev] = (cudaFuncGetAttributes(&at, reinterpret_cast<const void *>(kern)) == cudaSuccess &&
+                     at.numRegs == fa::BwdCfg<D>::kLaunchRegs)
+                        ? 1
+                        : -1;
+    }
+    if (usable[dev] < 0)
+      return fail(FA_ERR_CUDA, "bwd: kernel register count differs from its warpgroup split");
+  }
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
-  kern<<<grid, 384, smem, st>>>(tq, tk, tv, tdo, a);
+  kern<<<grid, fa::BwdCfg<D>::kThreads, smem, st>>>(tq, tk, tv, tdo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return FA_OK;

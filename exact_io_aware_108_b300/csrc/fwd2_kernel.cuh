@@ -279,14 +279,16 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait_warp(bar(C::kBOR + x), (t - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, m_new != m)) {
+          // all of the row in one TMEM round trip (a wait::ld costs ~600 cycles)
+          uint32_t o[D / 32][32];
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(ocol + c0, o);
-            tmem_wait_ld();
-            reg_fence_32(o);
-            scale32(o, alpha);
-            tmem_st_32x32b_x32(ocol + c0, o);
+          for (int j = 0; j < D / 32; ++j) tmem_ld_32x32b_x32(ocol + 32 * j, o[j]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {
+            reg_fence_32(o[j]);
+            scale32(o[j], alpha);
+            tmem_st_32x32b_x32(ocol + 32 * j, o[j]);
           }
         }
       }
@@ -305,17 +307,22 @@ __global__ void __launch_bounds__(384, 1)
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       uint16_t *orow = static_cast<uint16_t *>(a.o) +
                        (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
+      uint32_t oall[D / 32][32];
+      if (have_o) {
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) tmem_ld_32x32b_x32(ocol + 32 * j, oall[j]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) reg_fence_32(oall[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) oall[j][i] = 0u;
+      }
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        if (have_o) {
-          tmem_ld_32x32b_x32(ocol + c0, o);
-          tmem_wait_ld();
-          reg_fence_32(o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
+        const uint32_t (&o)[32] = oall[c0 / 32];
         uint32_t pk[16], rk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -195,6 +195,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Returns x through an opaque move: values derived from it are recomputed
+// where they are used instead of being hoisted out of a loop and held live
+// (the MMA issuer runs with few registers).
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
+}
+
 // Instruction descriptor, kind::f16, fp32 accumulator, dense.
 //   [4,6) D format 1 = f32; [7,10) A format, [10,13) B format (0 f16, 1 bf16);
 //   [15] A MN-major, [16] B MN-major; [17,23) N>>3; [24,29) M>>4.
