@@ -7,7 +7,9 @@
 // thread alternates between the tiles -- S_A = Q_A K_j^T, S_B = Q_B K_j^T,
 // O_A += P_A V_j, O_B += P_B V_j -- so while one warpgroup runs its softmax
 // the tensor cores work on the other tile. K_j and V_j are loaded once for
-// both tiles.
+// both tiles. The MMA issue order per key tile t is P_A V_t, S_A(t+1),
+// P_B V_t, S_B(t+1): each tile's next scores follow its own P V, so the
+// chain of one tile never waits for the other tile's softmax.
 //
 // Roles (384 threads; setmaxnreg moves registers from warpgroup 0 to the two
 // softmax warpgroups):
@@ -43,8 +45,8 @@ struct Fwd2Cfg {
   static constexpr int kBKE = kBVF + kStages;
   static constexpr int kBVE = kBKE + kStages;
   static constexpr int kBSF = kBVE + kStages;  // [2] S_X ready
-  static constexpr int kBPF = kBSF + 2;        // [2] P_X in TMEM (128 arrivals)
-  static constexpr int kBOR = kBPF + 2;        // [2] P_X V done
+  static constexpr int kBPF = kBSF + 2;        // [2][2] half h of P_X in TMEM (128 arrivals)
+  static constexpr int kBOR = kBPF + 4;        // [2] P_X V done
   static constexpr int kBDR = kBOR + 2;
   static constexpr int kNumBars = kBDR + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::kBSF + x), 1);
-      mbar_init(bar(C::kBPF + x), 128);
+      mbar_init(bar(C::kBPF + 2 * x), 128);
+      mbar_init(bar(C::kBPF + 2 * x + 1), 128);
       mbar_init(bar(C::kBOR + x), 1);
     }
     mbar_init(bar(C::kBDR), 1);
@@ -166,50 +169,70 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0 && n_max > 0) {
       constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_f16(BF16, 128, D, false, true);
-      bool ok = mbar_wait(bar(C::kBQ), 0, abort_flag);
+      // S_x(t) = Q_x K_t^T into TMEM; the caller has waited for K_t
+      auto issue_qk = [&](int x, int t) {
+        const uint32_t sb = opaque_u32(sbase);
+        const uint32_t kbase = sb + C::kKOff + (t % C::kStages) * C::kTileBytes;
+        const uint32_t qbase = sb + C::kQOff + x * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
+                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBSF + x));
+      };
+      // Per key tile t and query tile x: O_x += P_x V_t, then, once that
+      // product has read P_x out of S_x, S_x = Q_x K_{t+1}^T. Tile x's next
+      // scores do not wait for the other tile's softmax.
+      bool ok = mbar_wait(bar(C::kBQ), 0, abort_flag) && mbar_wait(bar(C::kBKF), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (n_tile[x] > 0) issue_qk(x, 0);
+        mma_commit(bar(C::kBKE));
+      }
       for (int t = 0; ok && t < n_max; ++t) {
         const int st = t % C::kStages;
         const uint32_t ph = (t / C::kStages) & 1;
-        if (!mbar_wait(bar(C::kBKF + st), ph, abort_flag)) { ok = false; break; }
-        const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (t >= n_tile[x]) continue;
-          // S_x still holds P_x of tile t - 1 until its P V is done
-          if (t >= 1 && !mbar_wait(bar(C::kBOR + x), (t - 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qbase = sbase + C::kQOff + x * C::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
-                   sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBSF + x));
-        }
-        if (!ok) break;
-        mma_commit(bar(C::kBKE + st));
+        const int st1 = (t + 1) % C::kStages;
+        const uint32_t ph1 = ((t + 1) / C::kStages) & 1;
         if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) { ok = false; break; }
-        const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
-#pragma unroll
+        const uint32_t vbase = opaque_u32(sbase) + C::kVOff + st * C::kTileBytes;
+        bool k_next = false;  // K_{t+1} waited for
+#pragma unroll 1
         for (int x = 0; x < 2; ++x) {
           if (t >= n_tile[x]) continue;
-          if (!mbar_wait(bar(C::kBPF + x), t & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
           const uint32_t ocol = tmem + C::kColO0 + x * D;
           const uint32_t pcol = tmem + C::col_s(x);
+          // P_x arrives in two halves of 64 keys; each half's products start
+          // as soon as it is in TMEM
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(bar(C::kBPF + 2 * x + h), t & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
-                   (t > 0 || ks > 0) ? 1u : 0u);
-          if constexpr (SPLIT) {
+            for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+              mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
+                     (t > 0 || ks > 0) ? 1u : 0u);
+            if constexpr (SPLIT) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
+              for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+                mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
+            }
           }
+          if (!ok) break;
           mma_commit(bar(C::kBOR + x));
+          if (t + 1 < n_tile[x]) {
+            // S_x holds P_x until this tile's P V is done
+            if ((!k_next && !mbar_wait(bar(C::kBKF + st1), ph1, abort_flag)) ||
+                !mbar_wait(bar(C::kBOR + x), t & 1, abort_flag)) { ok = false; break; }
+            k_next = true;
+            tc_fence_after();
+            issue_qk(x, t + 1);
+          }
         }
         if (!ok) break;
+        if (k_next) mma_commit(bar(C::kBKE + st1));
         mma_commit(bar(C::kBVE + st));
       }
       mma_commit(bar(C::kBDR));
@@ -264,37 +287,45 @@ __global__ void __launch_bounds__(384, 1)
       int limit = kvl - t * 128;
       if (CAUSAL && t == qt) limit = min(limit, row + 1);
       float m_new, alpha;
-      const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
-      l = l * alpha + rs;
+      const float nm = softmax_max<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      // rescale O_x first, so the P V of this tile can start right after the
+      // first half of P. S_x(t) complete implies P_x V of tile t - 1 is done:
+      // that product was finished before S_x(t) was issued.
+      if (t > 0 && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(ocol + 32 * j, o);
+          tmem_wait_ld();
+          reg_fence_32(o);
+          scale32(o, alpha);
+          tmem_st_32x32b_x32(ocol + 32 * j, o);
+        }
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      softmax_exp<0, 64>(s, sl2, nm, acc);
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t hi[16], lo[16];
         pack_p32<BF16, SPLIT>(s, c0, hi, lo);
         tmem_st_32x32b_x16(scol + c0 / 2, hi);
         if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
       }
-      // rescale O_x (after the scores are dead, to keep registers low); O_x
-      // holds P_x V of tiles < t once that MMA is done
-      if (t > 0) {
-        if (!mbar_wait_warp(bar(C::kBOR + x), (t - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, m_new != m)) {
-          // all of the row in one TMEM round trip (a wait::ld costs ~600 cycles)
-          uint32_t o[D / 32][32];
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBPF + 2 * x));
+      softmax_exp<64, 128>(s, sl2, nm, acc);
 #pragma unroll
-          for (int j = 0; j < D / 32; ++j) tmem_ld_32x32b_x32(ocol + 32 * j, o[j]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            reg_fence_32(o[j]);
-            scale32(o[j], alpha);
-            tmem_st_32x32b_x32(ocol + 32 * j, o[j]);
-          }
-        }
+      for (int c0 = 64; c0 < 128; c0 += 32) {
+        uint32_t hi[16], lo[16];
+        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+        tmem_st_32x32b_x16(scol + c0 / 2, hi);
+        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kBPF + x));
+      mbar_arrive(bar(C::kBPF + 2 * x + 1));
+      l = l * alpha + softmax_sum(acc);
       m = m_new;
     }
     // ---- epilogue: O / l and LSE (rows of a missing tile B are skipped)

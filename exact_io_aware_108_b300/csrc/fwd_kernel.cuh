@@ -209,18 +209,23 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
         const uint32_t pcol = tmem + (pb ? C::kColP1 : C::kColP0);
+        // two halves of 64 keys, high then low part of each (the product
+        // order of the two-tile kernel, so both round O identically)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
-          mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
-        }
-        if constexpr (SPLIT) {
-          const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
-                   kIdPV, 1u);
+          for (int ks = 4 * h; ks < 4 * h + 4; ++ks) {
+            // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
+            const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
+            mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
+          }
+          if constexpr (SPLIT) {
+            const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
+#pragma unroll
+            for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+              mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
+                     kIdPV, 1u);
+          }
         }
         mma_commit(bar(C::kBVE + st));
         mma_commit(bar(C::kBOR));

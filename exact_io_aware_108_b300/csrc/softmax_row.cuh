@@ -14,10 +14,11 @@
 
 namespace fa {
 
-// s: the 128 raw scores of this row (entries c >= limit are masked);
-// on return s holds p (fp32). Returns the tile's sum of p.
+// Masks entries c >= limit of s (the 128 raw scores of this row) and
+// moves the running max: returns -m_use, the offset of the exponent, and
+// sets m_new and alpha = 2^(m - m_new).
 template <bool LAZY>
-__device__ __forceinline__ float softmax_row(float (&s)[128], int limit, float sl2, float m,
+__device__ __forceinline__ float softmax_max(float (&s)[128], int limit, float sl2, float m,
                                              float &m_new, float &alpha) {
   if (limit < 128) {
 #pragma unroll
@@ -39,20 +40,39 @@ __device__ __forceinline__ float softmax_row(float (&s)[128], int limit, float s
   m_new = LAZY ? ((mxs > m + 8.0f) ? mxs : m) : fmaxf(m, mxs);
   const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
   alpha = ex2_approx(m - m_use);
-  const float nm = -m_use;
-  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  return -m_use;
+}
+
+// p_c = 2^(s_c * sl2 + nm) in place for columns [C0, C1) (a multiple of 4
+// wide), added into the four partial sums acc in a fixed order.
+template <int C0, int C1>
+__device__ __forceinline__ void softmax_exp(float (&s)[128], float sl2, float nm, float (&acc)[4]) {
 #pragma unroll
-  for (int c = 0; c < 128; c += 4) {
+  for (int c = C0; c < C1; c += 4) {
     ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, sl2, nm, nm);
     ffma2(s[c + 2], s[c + 3], s[c + 2], s[c + 3], sl2, sl2, nm, nm);
     s[c] = ex2_approx(s[c]);
     s[c + 1] = ex2_approx(s[c + 1]);
     s[c + 2] = ex2_approx(s[c + 2]);
     s[c + 3] = ex2_approx(s[c + 3]);
-    fadd2(a0, a1, a0, a1, s[c], s[c + 1]);
-    fadd2(b0, b1, b0, b1, s[c + 2], s[c + 3]);
+    fadd2(acc[0], acc[1], acc[0], acc[1], s[c], s[c + 1]);
+    fadd2(acc[2], acc[3], acc[2], acc[3], s[c + 2], s[c + 3]);
   }
-  return (a0 + a1) + (b0 + b1);
+}
+
+__device__ __forceinline__ float softmax_sum(const float (&acc)[4]) {
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// The whole row update: on return s holds p (fp32); returns the tile's sum
+// of p. Same arithmetic as softmax_max + softmax_exp<0, 128> + softmax_sum.
+template <bool LAZY>
+__device__ __forceinline__ float softmax_row(float (&s)[128], int limit, float sl2, float m,
+                                             float &m_new, float &alpha) {
+  const float nm = softmax_max<LAZY>(s, limit, sl2, m, m_new, alpha);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  softmax_exp<0, 128>(s, sl2, nm, acc);
+  return softmax_sum(acc);
 }
 
 // Packs p (fp32) of columns c0 .. c0+31 into 16 16-bit pairs (hi) and, for

@@ -4,7 +4,8 @@
         --dtype bf16 --causal --iters 2
 
 Inputs are seeded N(0,1) (Q and K times --qk-mult); the forward writes O's
-residual and the backward uses it, as in the benchmark.
+residual and the backward uses it, as in the benchmark (--plain: O and LSE
+only, the inference forward).
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ def main():
     ap.add_argument("--qk-mult", type=float, default=2.0)
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--plain", action="store_true", help="forward without O's residual")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     g = torch.Generator(device="cuda").manual_seed(0)
@@ -38,7 +40,11 @@ def main():
     scale = 1.0 / math.sqrt(a.d)
     ws = torch.empty(fa.fa_bwd_workspace_size(*shape), dtype=torch.uint8, device="cuda")
     for _ in range(a.iters):
-        o, lse, o_res = fa.attention_forward(q, k, v, scale, a.causal, return_residual=True)
+        if a.plain:
+            o, lse = fa.attention_forward(q, k, v, scale, a.causal)
+            o_res = None
+        else:
+            o, lse, o_res = fa.attention_forward(q, k, v, scale, a.causal, return_residual=True)
         if not a.fwd_only:
             fa.attention_backward(q, k, v, o, lse, do, scale, a.causal, o_res=o_res, workspace=ws)
     torch.cuda.synchronize()
