@@ -416,6 +416,78 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_configs(args):
+    """Per-workload forward / backward timings (one JSON line per workload).
+
+    Every workload of inputs.WORKLOADS, inputs resident on the device, CUDA
+    events around `args.steps` launches after `args.warmup`; no L2 flush (the
+    small workloads fit in L2). Forward with and without O's residual; the
+    backward is the whole fa_bwd (prepare, main, finish) with the residual.
+    """
+    import torch
+    import exact_io_aware_108_b300 as fa
+    from exact_io_aware_108_b300 import inputs
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if fa.fa_get_device_error() != 0:
+            raise RuntimeError("device error during the timed launches")
+        return e0.elapsed_time(e1) / args.steps
+
+    for name, w in inputs.WORKLOADS.items():
+        t = {k: v.to(dev) for k, v in inputs.make_workload(w, with_dout=True).items()}
+        q, k, v, dout = t["q"], t["k"], t["v"], t["dout"]
+        kl = t["kv_len"].to(torch.int32) if "kv_len" in t else None
+        bm = t.get("block_mask")
+        density = 1.0 if bm is None else float(bm.float().mean())
+        o, o_res = torch.empty_like(q), torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+        dq, dk, dvv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+
+        def fwd(res):
+            if bm is not None:
+                fa.fa_fwd_blocksparse(q, k, v, o, lse, w.scale, bm, o_res=res, stream=stream)
+            else:
+                fa.fa_fwd_ex(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res, stream=stream)
+
+        def bwd():
+            if bm is not None:
+                fa.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dvv, w.scale, bm, o_res, ws,
+                                      stream=stream)
+            else:
+                fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dvv, w.scale, w.causal, kl, o_res, ws,
+                          stream=stream)
+
+        ff = flops_fwd(w, density)
+        line = {"config": name, "density": round(density, 5), "fwd_gflop": round(ff / 1e9, 3)}
+        ms = timed(lambda: fwd(None))
+        line.update(fwd_ms=round(ms, 4), fwd_tflops=round(ff / ms / 1e9, 1))
+        ms = timed(lambda: fwd(o_res))
+        line.update(fwd_res_ms=round(ms, 4), fwd_res_tflops=round(ff / ms / 1e9, 1))
+        if w.backward:
+            fwd(o_res)
+            ms = timed(bwd)
+            line.update(bwd_ms=round(ms, 4), bwd_tflops=round(2.5 * ff / ms / 1e9, 1))
+        for key in ("fwd_tflops", "fwd_res_tflops", "bwd_tflops"):
+            if key in line:
+                line[key.replace("tflops", "frac_of_measured_burst")] = round(
+                    line[key] / peaks["bf16_tflops"], 4)
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,13 +495,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="time forward and backward of every workload (one JSON line each)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.configs:
+        run_configs(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)
