@@ -28,13 +28,13 @@
 //   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
 //                   query tile i through a two-stage ring.
 //   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
-//   warpgroups 1, 2 thread r owns key r for one 64-query half h of the tile:
-//                   P^T row -> TMEM (16-bit), dS^T row -> shared memory
-//                   (16-bit, scale folded in, computed from the fp32 P); at
-//                   the end warpgroup 1 writes dK, warpgroup 2 writes dV.
-//                   Each thread reads S^T and dP^T once per tile (one TMEM
-//                   round trip each), and the two warpgroups share each SM
-//                   sub-partition so one hides the other's TMEM latency.
+//   warpgroups 1, 2 one 64-query half h of the tile each: P^T -> TMEM
+//                   (16-bit), dS^T -> shared memory (16-bit, scale folded
+//                   in, computed from the fp32 P). A thread holds 4 keys x
+//                   16 queries (16-lane TMEM shapes), so it reads only 16 of
+//                   the half's per-query LSE and D values; at the end
+//                   warpgroup 1 writes dK, warpgroup 2 writes dV (one key
+//                   row per thread).
 //   warpgroup 3     reads the dQ partial from TMEM and adds it to the fp32
 //                   accumulator (d = 128: thread r owns head-dim channel r of
 //                   the transposed partial; d = 64: thread r owns query r).
@@ -416,59 +416,80 @@ __global__ void __launch_bounds__(512, 1)
     if (warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T, one query half
     const int h = (warp >> 2) - 1;  // query half: columns [64h, 64h+64) of the tile
-    const int r = tid & 127;         // key row within the tile
+    const int r = tid & 127;         // key row of this thread's lane (epilogue)
     const int key = kt * 128 + r;
-    const bool key_live = key < kvl;
     const float sl2 = a.scale_log2, scale = a.scale;
+    // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
+    // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
+    // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
+    // (i = 0, 1) of the tile, and for each column group b = 0..7 the query
+    // pair 8 b + 2 c4, +1 of this half. It therefore needs only 16 of the
+    // half's 64 per-query LSE and D values, read as 8 float2 each.
+    const int t4 = lane >> 2, c4 = lane & 3;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const uint32_t sDS = sbase + C::kdSOff + h * 16384;
-    const uint32_t col_s = tmem + lane_addr + C::kColS + 64 * h;
-    const uint32_t col_dp = tmem + lane_addr + C::kColDP + 64 * h;
     bool ok = true;
     int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
     for (int u = 0; u < n_iter; ++u) {
       const int st = u & 1;
-      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + C::kLseOff + st * 512 + h * 256);
-      const float4 *nd4 = reinterpret_cast<const float4 *>(smem + C::kDeltaOff + st * 512 + h * 256);
+      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + C::kLseOff + st * 512 + h * 256) + c4;
+      const float2 *nd2 = reinterpret_cast<const float2 *>(smem + C::kDeltaOff + st * 512 + h * 256) + c4;
       if (!mbar_wait_warp(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(bar(C::kBSF), u & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      // causal: query c of this tile sees key r iff qi*128 + c >= key; a dead
-      // key row sees nothing. Local column i is query 64h + i.
-      const int cmin = (!key_live ? 128 : (CAUSAL ? (key - qi * 128) : -1)) - 64 * h;
-      // P (fp32, kept in registers for dS) -> P^T (16-bit) into the first
-      // 32 columns of this half's S^T columns (already read), then dS^T.
-      float p[64];
+      // p[j][4b + 2i + e]: key (j, i), query 8b + 2c4 + e of this half, fp32,
+      // kept in registers for dS
+      float p[2][32];
       {
-        uint32_t s0[32], s1[32];
-        tmem_ld_32x32b_x32(col_s, s0);
-        tmem_ld_32x32b_x32(col_s + 32, s1);
+        uint32_t sv[2][32];
+        tmem_ld_16x256b_x8(tq + C::kColS + 64 * h, sv[0]);
+        tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColS + 64 * h, sv[1]);
         tmem_wait_ld();
-        reg_fence_32(s0);
-        reg_fence_32(s1);
+        reg_fence_32(sv[0]);
+        reg_fence_32(sv[1]);
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const float4 nl = nl4[i >> 2];
-          const uint32_t *src = i < 32 ? &s0[i] : &s1[i - 32];
-          ffma2(p[i], p[i + 1], __uint_as_float(src[0]), __uint_as_float(src[1]), sl2, sl2, nl.x, nl.y);
-          ffma2(p[i + 2], p[i + 3], __uint_as_float(src[2]), __uint_as_float(src[3]), sl2, sl2, nl.z,
-                nl.w);
-          p[i] = ex2_approx(p[i]);
-          p[i + 1] = ex2_approx(p[i + 1]);
-          p[i + 2] = ex2_approx(p[i + 2]);
-          p[i + 3] = ex2_approx(p[i + 3]);
-        }
-        if (cmin > 0) {  // some columns of this half are masked for this key
+        for (int b = 0; b < 8; ++b) {
+          const float2 nl = nl2[4 * b];
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i < cmin) p[i] = 0.f;
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int e = 4 * b + 2 * i;
+              ffma2(p[j][e], p[j][e + 1], __uint_as_float(sv[j][e]), __uint_as_float(sv[j][e + 1]), sl2,
+                    sl2, nl.x, nl.y);
+              p[j][e] = ex2_approx(p[j][e]);
+              p[j][e + 1] = ex2_approx(p[j][e + 1]);
+            }
         }
+        // causal: query c of this tile sees key k iff qi*128 + c >= kt*128 + k;
+        // a dead key sees nothing. Local column 8b + 2c4 + e is query
+        // 64h + 8b + 2c4 + e of the tile.
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int kk = kt * 128 + 32 * (warp & 3) + 16 * j + 8 * i + t4;
+            const int cmin = (kk >= kvl ? 128 : (CAUSAL ? (kk - qi * 128) : -1)) - 64 * h;
+            if (cmin > 0) {
+#pragma unroll
+              for (int b = 0; b < 8; ++b)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  if (8 * b + 2 * c4 + e < cmin) p[j][4 * b + 2 * i + e] = 0.f;
+            }
+          }
       }
+      // P^T (16-bit pairs, column = query pair) into the first 32 columns of
+      // this half's S^T columns (already read)
 #pragma unroll
-      for (int c0 = 0; c0 < 32; c0 += 16) {
+      for (int j = 0; j < 2; ++j) {
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack2<BF16>(p[2 * (c0 + i)], p[2 * (c0 + i) + 1]);
-        tmem_st_32x32b_x16(col_s + c0, w);
+        for (int b = 0; b < 8; ++b) {
+          w[2 * b] = pack2<BF16>(p[j][4 * b], p[j][4 * b + 1]);
+          w[2 * b + 1] = pack2<BF16>(p[j][4 * b + 2], p[j][4 * b + 3]);
+        }
+        tmem_st_16x128b_x8(tq + (static_cast<uint32_t>(16 * j) << 16) + C::kColS + 64 * h, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -477,38 +498,32 @@ __global__ void __launch_bounds__(512, 1)
       // the previous dQ/dK MMAs must be done reading dS before it is rewritten
       if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t d0[32], d1[32];
-      tmem_ld_32x32b_x32(col_dp, d0);
-      tmem_ld_32x32b_x32(col_dp + 32, d1);
+      uint32_t dv[2][32];
+      tmem_ld_16x256b_x8(tq + C::kColDP + 64 * h, dv[0]);
+      tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColDP + 64 * h, dv[1]);
       tmem_wait_ld();
-      reg_fence_32(d0);
-      reg_fence_32(d1);
+      reg_fence_32(dv[0]);
+      reg_fence_32(dv[1]);
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        const uint32_t *dr = c0 == 0 ? d0 : d1;
-        uint32_t w[16];
+      for (int b = 0; b < 8; ++b) {
+        const float2 nd = nd2[4 * b];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
-          const float4 nd = nd4[(c0 + i) >> 2];
-          float t0, t1, t2, t3;
-          ffma2(t0, t1, __uint_as_float(dr[i]), __uint_as_float(dr[i + 1]), scale, scale, nd.x, nd.y);
-          ffma2(t2, t3, __uint_as_float(dr[i + 2]), __uint_as_float(dr[i + 3]), scale, scale, nd.z, nd.w);
-          fmul2(t0, t1, t0, t1, p[c0 + i], p[c0 + i + 1]);
-          fmul2(t2, t3, t2, t3, p[c0 + i + 2], p[c0 + i + 3]);
-          w[i / 2] = pack2<BF16>(t0, t1);
-          w[i / 2 + 1] = pack2<BF16>(t2, t3);
-        }
-        // row r of the dS^T tile, queries 64h+c0 .. +31 = 4 16-byte chunks of
-        // the 128-byte row in region h, swizzled by (r & 7)
-        const uint32_t rowb = sDS + r * 128;
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint32_t chunk = ((c0 >> 3) + v) ^ (r & 7);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + chunk * 16),
-                       "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3])
-                       : "memory");
-        }
+          for (int i = 0; i < 2; ++i) {
+            // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
+            const int e = 4 * b + 2 * i;
+            float t0, t1;
+            ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), scale, scale, nd.x,
+                  nd.y);
+            fmul2(t0, t1, t0, t1, p[j][e], p[j][e + 1]);
+            // row = key of the dS^T tile; queries 8b + 2c4, +1 are the 4-byte
+            // word c4 of 16-byte chunk b of the row's 128 bytes in region h,
+            // swizzled by (row & 7) = t4
+            const int row = 32 * (warp & 3) + 16 * j + 8 * i + t4;
+            const uint32_t addr = sDS + row * 128 + ((b ^ t4) << 4) + 4 * c4;
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<BF16>(t0, t1)) : "memory");
+          }
       }
       fence_proxy_async_smem();
       tc_fence_before();
