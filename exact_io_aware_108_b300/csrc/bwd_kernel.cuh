@@ -63,6 +63,7 @@ struct BwdArgs {
   const int32_t *kv_len;
   const uint8_t *block_mask;
   int H, N, nqt, nkt;
+  int hgroup;  // heads per scheduling group (causal launch order, see below)
   float scale, scale_log2;
 };
 
@@ -217,8 +218,19 @@ __global__ void __launch_bounds__(512, 1)
   volatile uint32_t *abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
 
-  const int bh = blockIdx.x / a.nkt;
-  const int kt = blockIdx.x % a.nkt;  // causal: low key tiles carry the most work, run first
+  // Launch order: groups of hgroup heads; within a group key tile major,
+  // so the heaviest CTAs of the group (causal: low key tiles see the most
+  // query tiles) start first, while the heads that run concurrently stay
+  // few enough for their Q and dO to stay in L2.
+  int bh, kt;
+  {
+    const int BH = static_cast<int>(gridDim.x) / a.nkt;
+    const int grp = static_cast<int>(blockIdx.x) / (a.hgroup * a.nkt);
+    const int rem = static_cast<int>(blockIdx.x) - grp * a.hgroup * a.nkt;
+    const int nh = min(a.hgroup, BH - grp * a.hgroup);
+    kt = rem / nh;
+    bh = grp * a.hgroup + rem % nh;
+  }
   const int b = bh / a.H;
   int kvl = a.N;
   if (a.kv_len != nullptr) {

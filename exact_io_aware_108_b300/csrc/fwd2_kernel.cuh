@@ -77,10 +77,21 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
 
   // ---- work item: 256 query rows (tiles 2qb, 2qb+1) of one head
+  // Launch order: groups of hgroup heads; within a group query-block
+  // major, heaviest first (causal: the last blocks see the most key tiles),
+  // while the heads that run concurrently stay few enough for their K and V
+  // to stay in L2.
   const int nqb = (a.nqt + 1) >> 1;
-  const int bh = blockIdx.x / nqb;
-  int qb = blockIdx.x % nqb;
-  if (CAUSAL) qb = nqb - 1 - qb;  // heaviest blocks first
+  int bh, qb;
+  {
+    const int BH = static_cast<int>(gridDim.x) / nqb;
+    const int grp = static_cast<int>(blockIdx.x) / (a.hgroup * nqb);
+    const int rem = static_cast<int>(blockIdx.x) - grp * a.hgroup * nqb;
+    const int nh = min(a.hgroup, BH - grp * a.hgroup);
+    qb = rem / nh;
+    bh = grp * a.hgroup + rem % nh;
+  }
+  if (CAUSAL) qb = nqb - 1 - qb;
   const int b = bh / a.H;
   int kvl = a.N;
   if (a.kv_len != nullptr) {

@@ -44,6 +44,7 @@ struct FwdArgs {
   const int32_t *kv_len;     // [B] or null
   const uint8_t *block_mask; // [nkt, nkt] or null
   int H, N, nqt, nkt;
+  int hgroup;  // heads per scheduling group of the two-tile kernel's causal launch order
   float scale_log2;
 };
 
