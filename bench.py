@@ -40,10 +40,10 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources hashed in "source_sha256"; see profiles/.
 TRAFFIC = {
-    "source_sha256": "f53ac2cd1f21fa1af87da3a7f448915e924f51226fd58f5154f9e389f0d76d31",
+    "source_sha256": "c356a8c2222679729c4edf899d0ec727c1883788d58c70e2e54fdca7e4a134ce",
     # measured on B/4 of each sweep point (ncu, one launch) and scaled by 4 (DRAM
     # bytes grow with the number of heads): see profiles/bwd_main_kernel_*.md
-    "bytes_per_launch": {"4096": 4 * 286996736, "8192": 4 * 286693632, "16384": 4 * 289037056},
+    "bytes_per_launch": {"4096": 4 * 290137088, "8192": 4 * 373601280, "16384": 4 * 395916288},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
