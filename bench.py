@@ -454,12 +454,15 @@ def run_configs(args):
         density = 1.0 if bm is None else float(bm.float().mean())
         o, o_res = torch.empty_like(q), torch.empty_like(q)
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
-        dq, dk, dvv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        gqa = w.hkv is not None and w.hkv != w.H
         ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
 
         def fwd(res):
             if bm is not None:
                 fa.fa_fwd_blocksparse(q, k, v, o, lse, w.scale, bm, o_res=res, stream=stream)
+            elif gqa:
+                fa.fa_fwd_gqa(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res, stream=stream)
             else:
                 fa.fa_fwd_ex(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res, stream=stream)
 
@@ -467,6 +470,9 @@ def run_configs(args):
             if bm is not None:
                 fa.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dvv, w.scale, bm, o_res, ws,
                                       stream=stream)
+            elif gqa:
+                fa.fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dvv, w.scale, w.causal, kl, o_res, ws,
+                              stream=stream)
             else:
                 fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dvv, w.scale, w.causal, kl, o_res, ws,
                           stream=stream)

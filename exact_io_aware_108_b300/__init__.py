@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     fa_bwd,
     fa_bwd_blocksparse,
     fa_bwd_finish,
+    fa_bwd_gqa,
     fa_bwd_main,
     fa_bwd_noalloc,
     fa_bwd_noalloc_max_workspace,
@@ -19,6 +20,7 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_blocksparse,
     fa_fwd_ex,
+    fa_fwd_gqa,
     fa_get_device_error,
     fa_last_error_message,
     fa_status_str,

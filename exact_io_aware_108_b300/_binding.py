@@ -18,8 +18,8 @@ FA_F16, FA_BF16 = 0, 1
 
 # every symbol include/fa.h declares
 EXPORTS = (
-    "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_bwd_workspace_size", "fa_bwd",
-    "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
+    "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_bwd_workspace_size", "fa_bwd",
+    "fa_bwd_gqa", "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace",
     "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
 )
@@ -62,11 +62,14 @@ def load_library():
         lib.fa_fwd_ex.argtypes = fwd + [_vp, _vp, _vp]
         lib.fa_fwd_blocksparse.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp,
                                            _vp]
+        lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp,
+                                   _vp]
         lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_bwd_workspace_size.restype = _sz
         bwd = [_vp] * 9 + [_i, _i, _i, _i, _f]
         lib.fa_bwd.argtypes = bwd + [_i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_blocksparse.argtypes = bwd + [_i, _vp, _vp, _vp, _sz, _vp]
+        lib.fa_bwd_gqa.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd_main.argtypes = [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_finish.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
@@ -81,7 +84,8 @@ def load_library():
         lib.fa_last_error_message.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_blocksparse",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_bwd", "fa_bwd_gqa",
+                     "fa_bwd_blocksparse",
                      "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
             getattr(lib, name).restype = _i
         _lib = lib
@@ -154,6 +158,16 @@ def fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, o_res=None, stream=No
            "fa_fwd_blocksparse")
 
 
+def fa_fwd_gqa(q, k, v, o, lse, scale, causal=False, kv_len=None, o_res=None, stream=None):
+    """q, o [B, H, N, d]; k, v [B, Hkv, N, d] (H a multiple of Hkv)."""
+    B, H, N, d = _dims(q)
+    Hkv = int(k.shape[1])
+    _check(load_library().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                     float(scale), int(bool(causal)), _dtype_code(q), _ptr(kv_len),
+                                     _ptr(o_res), _stream(stream)),
+           "fa_fwd_gqa")
+
+
 def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
@@ -168,6 +182,19 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal=False, kv_len=None, 
                                  int(bool(causal)), _dtype_code(q), _ptr(kv_len), _ptr(o_res),
                                  _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "fa_bwd")
+
+
+def fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, scale, causal=False, kv_len=None, o_res=None,
+               workspace=None, workspace_bytes=None, stream=None):
+    """dq [B, H, N, d]; dk, dv [B, Hkv, N, d], summed over each group of query heads."""
+    B, H, N, d = _dims(q)
+    Hkv = int(k.shape[1])
+    _check(load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d, float(scale),
+                                     int(bool(causal)), _dtype_code(q), _ptr(kv_len), _ptr(o_res),
+                                     _ptr(workspace), _ws_bytes(workspace, workspace_bytes),
+                                     _stream(stream)),
+           "fa_bwd_gqa")
 
 
 def fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, o_res=None,

@@ -12,8 +12,10 @@ def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask
                       return_residual=False, stream=None):
     """O [B,H,N,d] and LSE [B,H,N] fp32 of exact attention (device tensors).
 
-    With return_residual=True also returns O's rounding residual (same dtype),
-    which attention_backward uses for a more accurate D = rowsum(dO * O)."""
+    k and v may have fewer heads than q (grouped-query attention: [B,Hkv,N,d]
+    with H a multiple of Hkv). With return_residual=True also returns O's
+    rounding residual (same dtype), which attention_backward uses for a more
+    accurate D = rowsum(dO * O)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     o = torch.empty_like(q)
@@ -21,6 +23,8 @@ def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask
     o_res = torch.empty_like(q) if return_residual else None
     if block_mask is not None:
         B.fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, o_res=o_res, stream=stream)
+    elif k.shape[1] != q.shape[1]:
+        B.fa_fwd_gqa(q, k, v, o, lse, scale, causal, kv_len, o_res=o_res, stream=stream)
     elif kv_len is not None or o_res is not None:
         B.fa_fwd_ex(q, k, v, o, lse, scale, causal, kv_len, o_res=o_res, stream=stream)
     else:
@@ -30,7 +34,8 @@ def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask
 
 def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=None,
                        block_mask=None, o_res=None, workspace=None, stream=None):
-    """dQ, dK, dV [B,H,N,d] of exact attention (device tensors)."""
+    """dQ, dK, dV of exact attention (device tensors); dK and dV have k's shape
+    (grouped-query attention: summed over each group of query heads)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     Bsz, H, N, d = q.shape
@@ -43,6 +48,9 @@ def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=N
     if block_mask is not None:
         B.fa_bwd_blocksparse(q, k, v, o, lse, dout, dq, dk, dv, scale, block_mask, o_res=o_res,
                              workspace=workspace, stream=stream)
+    elif k.shape[1] != q.shape[1]:
+        B.fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, kv_len, o_res=o_res,
+                     workspace=workspace, stream=stream)
     else:
         B.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, kv_len, o_res=o_res,
                  workspace=workspace, stream=stream)

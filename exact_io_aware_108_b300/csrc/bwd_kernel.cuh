@@ -16,9 +16,12 @@
 //                    uses O plus its rounding residual when the forward
 //                    wrote one: with bf16 O alone the rounding of O moves
 //                    D_i by up to ~0.05 at d = 128, which reaches dQ and dK.
-//   bwd_main_kernel  one CTA per 128-key tile of one (batch, head); K_j, V_j
-//                    stay in shared memory, dK_j and dV_j stay in TMEM, and
-//                    the CTA loops over the query tiles that see key tile j.
+//   bwd_main_kernel  one CTA per 128-key tile of one (batch, key/value head);
+//                    K_j, V_j stay in shared memory, dK_j and dV_j stay in
+//                    TMEM, and the CTA loops over the query tiles that see
+//                    key tile j, of every query head that reads this
+//                    key/value head (one head unless the attention is
+//                    grouped-query).
 //                    The scores are computed transposed (keys on TMEM lanes)
 //                    so P^T and dS^T are row-local to one thread per key.
 //   bwd_dq_kernel    dQ accumulator (fp32) -> dQ (fp16/bf16).
@@ -63,8 +66,14 @@ struct BwdArgs {
   const int32_t *kv_len;
   const uint8_t *block_mask;
   int H, N, nqt, nkt;
-  int hgroup;  // heads per scheduling group (causal launch order, see below)
+  int hgroup;    // heads per scheduling group (causal launch order, see below)
+  int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
+  int kv_group;  // query heads per key/value head
   float scale, scale_log2;
+  // [B*H] index of query head g of the group that reads key/value head bkv
+  __device__ __forceinline__ int q_head(int bkv, int g) const {
+    return (bkv / Hkv) * H + (bkv % Hkv) * kv_group + g;
+  }
 };
 
 // 1-D bulk copy global -> shared, completion as transaction bytes on bar.
@@ -222,16 +231,16 @@ __global__ void __launch_bounds__(512, 1)
   // so the heaviest CTAs of the group (causal: low key tiles see the most
   // query tiles) start first, while the heads that run concurrently stay
   // few enough for their Q and dO to stay in L2.
-  int bh, kt;
+  int bkv, kt;  // key/value head ([B*Hkv] index) and key tile of this CTA
   {
     const int BH = static_cast<int>(gridDim.x) / a.nkt;
     const int grp = static_cast<int>(blockIdx.x) / (a.hgroup * a.nkt);
     const int rem = static_cast<int>(blockIdx.x) - grp * a.hgroup * a.nkt;
     const int nh = min(a.hgroup, BH - grp * a.hgroup);
     kt = rem / nh;
-    bh = grp * a.hgroup + rem % nh;
+    bkv = grp * a.hgroup + rem % nh;
   }
-  const int b = bh / a.H;
+  const int b = bkv / a.Hkv;
   int kvl = a.N;
   if (a.kv_len != nullptr) {
     const int v = a.kv_len[b];
@@ -248,6 +257,17 @@ __global__ void __launch_bounds__(512, 1)
       n_iter = a.nqt - q_begin;
     }
   }
+  // grouped-query attention: the CTA walks every query head of its group,
+  // (g, qi) in order, accumulating their dK and dV in TMEM
+  n_iter *= a.kv_group;
+  const int q_first = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+  auto advance = [&](int &g, int &qi) {
+    qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+    if (qi >= a.nqt) {
+      ++g;
+      qi = q_first;
+    }
+  };
 
   if (tid == 0) {
     mbar_init(bar(C::kBKV), 1);
@@ -290,10 +310,10 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t pol_q = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBKV), 2 * C::kTileBytes);
       for (int kb = 0; kb < C::kKB; ++kb) {
-        tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKV), kb * 64, kt * 128, bh, pol_kv);
-        tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBKV), kb * 64, kt * 128, bh, pol_kv);
+        tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKV), kb * 64, kt * 128, bkv, pol_kv);
+        tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBKV), kb * 64, kt * 128, bkv, pol_kv);
       }
-      int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+      int g = 0, qi = q_first;
       int issued = 0;
       for (int u = 0; u < n_iter; ++u) {
         const int st = u & 1;
@@ -301,15 +321,15 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive_expect_tx(bar(C::kBQF + st), 2 * C::kTileBytes + 1024);
         for (int kb = 0; kb < C::kKB; ++kb) {
           tma_load_3d_hint(sbase + C::kQOff + st * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQF + st),
-                           kb * 64, qi * 128, bh, pol_q);
+                           kb * 64, qi * 128, a.q_head(bkv, g), pol_q);
           tma_load_3d_hint(sbase + C::kdOOff + st * C::kTileBytes + kb * 16384, &tm_do,
-                           bar(C::kBQF + st), kb * 64, qi * 128, bh, pol_q);
+                           bar(C::kBQF + st), kb * 64, qi * 128, a.q_head(bkv, g), pol_q);
         }
-        const long long r0 = bh * tile_rows + static_cast<long long>(qi) * 128;
+        const long long r0 = a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128;
         bulk_load(sbase + C::kLseOff + st * 512, a.lse_l2 + r0, 512, bar(C::kBQF + st));
         bulk_load(sbase + C::kDeltaOff + st * 512, a.delta + r0, 512, bar(C::kBQF + st));
         issued = u + 1;
-        qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+        advance(g, qi);
       }
       if (*abort_flag) {
         mbar_wait_drain(bar(C::kBKV), 0, abort_flag);
@@ -441,7 +461,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const uint32_t sDS = sbase + C::kdSOff + h * 16384;
     bool ok = true;
-    int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+    int g = 0, qi = q_first;
     for (int u = 0; u < n_iter; ++u) {
       const int st = u & 1;
       const float2 *nl2 = reinterpret_cast<const float2 *>(smem + C::kLseOff + st * 512 + h * 256) + c4;
@@ -540,7 +560,7 @@ __global__ void __launch_bounds__(512, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kBDSR));
-      qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+      advance(g, qi);
     }
     // ---- epilogue: warpgroup 1 writes dK, warpgroup 2 writes dV
     bool have = ok && n_iter > 0;
@@ -549,7 +569,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_after();
     }
     uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
-                    (static_cast<size_t>(bh) * a.N + static_cast<size_t>(key)) * D;
+                    (static_cast<size_t>(bkv) * a.N + static_cast<size_t>(key)) * D;
     uint32_t v[D / 32][32];
     if (have) {
 #pragma unroll
@@ -579,7 +599,7 @@ __global__ void __launch_bounds__(512, 1)
     } else {
     // ------------------------------------------------------------ dQ partials
     const int r = tid & 127;  // d = 128: head-dim channel; d = 64: query row
-    int qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
+    int g = 0, qi = q_first;
     for (int u = 0; u < n_iter; ++u) {
       if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
       tc_fence_after();
@@ -601,7 +621,7 @@ __global__ void __launch_bounds__(512, 1)
         // pause after every 16 keeps the sub-partition's memory-instruction
         // queue from filling, so the softmax warpgroups' shared-memory
         // accesses behind it are not held up (measured 4-5 % faster).
-        float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128) * D + r;
+        float *acc = a.dq_acc + (a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128) * D + r;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -614,7 +634,7 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
       } else {
-        float *acc = a.dq_acc + (bh * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
+        float *acc = a.dq_acc + (a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j)
 #pragma unroll
@@ -623,7 +643,7 @@ __global__ void __launch_bounds__(512, 1)
                       make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
                                   __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
       }
-      qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+      advance(g, qi);
     }
     }
     // teardown of the compute warpgroups

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -209,12 +210,24 @@ fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   return launch_fwd_s<D, BF16, false>(tq, tk, tv, a, grid, causal, sparse, st);
 }
 
+// Hkv: key/value heads (0 = H); H must be a multiple of it (grouped-query
+// attention: query head h reads key/value head h / (H / Hkv)).
+fa_status check_kv_heads(int H, int *Hkv, bool sparse) {
+  if (*Hkv == 0) *Hkv = H;
+  if (*Hkv < 1 || *Hkv > H || H % *Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "Hkv=%d must divide H=%d", *Hkv, H);
+  if (sparse && *Hkv != H) return fail(FA_ERR_UNSUPPORTED, "block-sparse attention needs Hkv == H");
+  return FA_OK;
+}
+
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int N, int d, float scale, int causal, fa_dtype dt, const int32_t *kv_len,
-                   const uint8_t *block_mask, bool sparse, void *o_res, void *stream) {
+                   const uint8_t *block_mask, bool sparse, void *o_res, void *stream, int Hkv = 0) {
   Shape s;
   fa_status r = check_common(B, H, N, d, scale, dt, &s);
   if (r != FA_OK) return r;
+  if ((r = check_kv_heads(H, &Hkv, sparse)) != FA_OK) return r;
+  const long long BHkv = static_cast<long long>(B) * Hkv;
   r = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
   if (r != FA_OK) return r;
   if (sparse) {
@@ -228,8 +241,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     return fail(FA_ERR_INVALID_ARG, "o_res is not 16-byte aligned");
   CUtensorMap tq, tk, tv;
   if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
-  if ((r = make_tile_map(&tk, k, dt, N, s.BH, d, "k")) != FA_OK) return r;
-  if ((r = make_tile_map(&tv, v, dt, N, s.BH, d, "v")) != FA_OK) return r;
+  if ((r = make_tile_map(&tk, k, dt, N, BHkv, d, "k")) != FA_OK) return r;
+  if ((r = make_tile_map(&tv, v, dt, N, BHkv, d, "v")) != FA_OK) return r;
   fa::FwdArgs a;
   a.o = o;
   a.o_res = o_res;
@@ -241,6 +254,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.nqt = s.nqt;
   a.nkt = s.nqt;
   a.hgroup = head_group(N, d, causal != 0);
+  a.Hkv = Hkv;
+  a.kv_group = H / Hkv;
   a.scale_log2 = scale * 1.4426950408889634f;
   const int grid = static_cast<int>(s.BH * s.nqt);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -339,10 +354,12 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
                    const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
                    float scale, int causal, fa_dtype dt, const int32_t *kv_len,
                    const uint8_t *block_mask, bool sparse, const void *o_res, void *workspace,
-                   size_t ws_bytes, void *stream, unsigned phases = kAll) {
+                   size_t ws_bytes, void *stream, unsigned phases = kAll, int Hkv = 0) {
   Shape s;
   fa_status r = check_common(B, H, N, d, scale, dt, &s);
   if (r != FA_OK) return r;
+  if ((r = check_kv_heads(H, &Hkv, sparse)) != FA_OK) return r;
+  const long long BHkv = static_cast<long long>(B) * Hkv;
   // each phase reads/writes only some of the tensors
   if (phases & kPrepare) {
     r = check_ptrs({{o, "o"}, {lse, "lse"}, {dout, "dout"}});
@@ -371,8 +388,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   CUtensorMap tq, tk, tv, tdo;
   if (phases & kMain) {
     if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
-    if ((r = make_tile_map(&tk, k, dt, N, s.BH, d, "k")) != FA_OK) return r;
-    if ((r = make_tile_map(&tv, v, dt, N, s.BH, d, "v")) != FA_OK) return r;
+    if ((r = make_tile_map(&tk, k, dt, N, BHkv, d, "k")) != FA_OK) return r;
+    if ((r = make_tile_map(&tv, v, dt, N, BHkv, d, "v")) != FA_OK) return r;
     if ((r = make_tile_map(&tdo, dout, dt, N, s.BH, d, "dout")) != FA_OK) return r;
   }
   const size_t rows = padded_rows(B, H, N);
@@ -394,12 +411,15 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.N = N;
   a.nqt = s.nqt;
   a.nkt = s.nqt;
-  a.hgroup = head_group(N, d, causal != 0);
+  a.Hkv = Hkv;
+  a.kv_group = H / Hkv;
+  // a CTA streams the Q and dO of all kv_group query heads of its group
+  a.hgroup = std::max(1, head_group(N, d, causal != 0) / a.kv_group);
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   const long long rows_pad = static_cast<long long>(rows);
   const long long n_vec4 = s.BH * static_cast<long long>(N) * d / 4;
-  const int grid = static_cast<int>(s.BH * s.nqt);
+  const int grid = static_cast<int>(BHkv * s.nqt);  // one CTA per (batch, key/value head, key tile)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
   if (d == 64)
@@ -464,6 +484,14 @@ fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *
                   stream);
 }
 
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int Hkv, int N, int d, float scale, int causal, fa_dtype dtype,
+                     const int32_t *kv_len, void *o_res, void *stream) {
+  if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
+                  o_res, stream, Hkv);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   return fa_bwd_ws_bytes(B, H, N, d);
@@ -475,6 +503,15 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  void *workspace, size_t workspace_bytes, void *stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, dtype, kv_len,
                   nullptr, false, o_res, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N,
+                     int d, float scale, int causal, fa_dtype dtype, const int32_t *kv_len,
+                     const void *o_res, void *workspace, size_t workspace_bytes, void *stream) {
+  if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, dtype, kv_len,
+                  nullptr, false, o_res, workspace, workspace_bytes, stream, kAll, Hkv);
 }
 
 fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,

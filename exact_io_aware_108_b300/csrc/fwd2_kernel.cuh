@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   if (CAUSAL) qb = nqb - 1 - qb;
   const int b = bh / a.H;
+  const int kvh = a.kv_head(bh);
   int kvl = a.N;
   if (a.kv_len != nullptr) {
     const int v = a.kv_len[b];
@@ -158,13 +159,13 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
-                           bar(C::kBKF + st), kb * 64, t * 128, bh, pol_kv);
+                           bar(C::kBKF + st), kb * 64, t * 128, kvh, pol_kv);
         nk = t + 1;
         if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
-                           bar(C::kBVF + st), kb * 64, t * 128, bh, pol_kv);
+                           bar(C::kBVF + st), kb * 64, t * 128, kvh, pol_kv);
         nv = t + 1;
       }
       if (*abort_flag) {

@@ -44,8 +44,12 @@ struct FwdArgs {
   const int32_t *kv_len;     // [B] or null
   const uint8_t *block_mask; // [nkt, nkt] or null
   int H, N, nqt, nkt;
-  int hgroup;  // heads per scheduling group of the two-tile kernel's causal launch order
+  int hgroup;    // heads per scheduling group of the two-tile kernel's causal launch order
+  int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
+  int kv_group;  // query heads per key/value head
   float scale_log2;
+  // [B*Hkv] index of the key/value head that query head bh ([B*H] index) reads
+  __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
 };
 
 template <int D>
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(256, 1)
   int qt = blockIdx.x % a.nqt;
   if (CAUSAL) qt = a.nqt - 1 - qt;
   const int b = bh / a.H;
+  const int kvh = a.kv_head(bh);
   int kvl = a.N;
   if (a.kv_len != nullptr) {
     const int v = a.kv_len[b];
@@ -176,13 +181,13 @@ __global__ void __launch_bounds__(256, 1)
         mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
-                           bar(C::kBKF + st), kb * 64, kt * 128, bh, pol_kv);
+                           bar(C::kBKF + st), kb * 64, kt * 128, kvh, pol_kv);
         nk = t + 1;
         if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
-                           bar(C::kBVF + st), kb * 64, kt * 128, bh, pol_kv);
+                           bar(C::kBVF + st), kb * 64, kt * 128, kvh, pol_kv);
         nv = t + 1;
       }
       if (*abort_flag) {

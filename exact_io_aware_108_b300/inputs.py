@@ -40,6 +40,7 @@ class Workload:
     qk_mult: float = 1.0
     seed: int = 0
     backward: bool = True
+    hkv: int | None = None            # key/value heads (grouped-query attention), None = H
     notes: str = field(default="", compare=False)
 
     @property
@@ -68,18 +69,23 @@ WORKLOADS = {
         qk_mult=2.0),
     "blocksparse_b2_h8_n16384_d64_f16": Workload(
         "blocksparse_b2_h8_n16384_d64_f16", 2, 8, 16384, 64, "f16", block_sparse_p=0.2),
+    # grouped-query attention (32 query heads sharing 8 key/value heads)
+    "gqa_b4_h32_hkv8_n4096_d128_bf16_causal": Workload(
+        "gqa_b4_h32_hkv8_n4096_d128_bf16_causal", 4, 32, 4096, 128, "bf16", causal=True, hkv=8),
 }
 
 
 def make_qkv(B, H, N, d, dtype, seed=0, qk_mult=1.0, with_dout=True,
-             kv_len_range=None):
-    """Draw q, k, v (and dO, kv_len) on the CPU. Returns a dict of tensors."""
+             kv_len_range=None, hkv=None):
+    """Draw q, k, v (and dO, kv_len) on the CPU. Returns a dict of tensors.
+    hkv: number of key/value heads (k, v are [B, hkv, N, d]); None = H."""
     tdt = torch.float16 if dtype in ("f16", torch.float16) else torch.bfloat16
     g = torch.Generator(device="cpu").manual_seed(seed)
     shape = (B, H, N, d)
+    kv_shape = (B, H if hkv is None else hkv, N, d)
     q = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
-    k = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
-    v = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32).to(tdt)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32).to(tdt)
     out = {"q": q, "k": k, "v": v}
     if with_dout or kv_len_range is not None:
         out["dout"] = torch.randn(shape, generator=g, dtype=torch.float32).to(tdt)
@@ -107,7 +113,7 @@ def make_workload(w: Workload, with_dout=None):
     if with_dout is None:
         with_dout = w.backward
     t = make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult,
-                 with_dout=with_dout, kv_len_range=w.kv_len_range)
+                 with_dout=with_dout, kv_len_range=w.kv_len_range, hkv=w.hkv)
     if w.block_sparse_p is not None:
         t["block_mask"] = make_block_mask(w.N, w.block_sparse_p, seed=w.mask_seed)
     return t

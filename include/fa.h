@@ -116,6 +116,21 @@ fa_status fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *
                              void *stream);
 
 /*
+ * Grouped-query (and multi-query) forward: Hkv key/value heads shared by
+ * groups of H / Hkv query heads, query head h reading key/value head
+ * h / (H / Hkv). The FlashAttention-2 page ("Flash Attention:
+ * revolutionizing transformer efficiency", section FlashAttention-2) lists
+ * multi-query and grouped-query attention among its additions; the
+ * arithmetic per head is that of fa_fwd_ex.
+ *   q, o [B,H,N,d]; k, v [B,Hkv,N,d]; lse [B,H,N]; kv_len, o_res as in
+ *   fa_fwd_ex. 1 <= Hkv <= H and H % Hkv == 0, else FA_ERR_INVALID_ARG.
+ *   Hkv == H is fa_fwd_ex.
+ */
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int Hkv, int N, int d, float scale, int causal,
+                     fa_dtype dtype, const int32_t *kv_len, void *o_res, void *stream);
+
+/*
  * Bytes of device workspace fa_bwd / fa_bwd_blocksparse need for these
  * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
  * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ
@@ -145,6 +160,20 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
                  const int32_t *kv_len, const void *o_res, void *workspace,
                  size_t workspace_bytes, void *stream);
+
+/*
+ * Grouped-query backward (the gradients of fa_fwd_gqa): dq [B,H,N,d] per
+ * query head; dk, dv [B,Hkv,N,d], each the sum over the H / Hkv query heads
+ * that read that key/value head. One CTA per (batch, key/value head, key
+ * tile) walks every query head of its group, so dK and dV are accumulated
+ * on chip and stay deterministic. Other arguments as in fa_bwd; the
+ * workspace is fa_bwd_workspace_size(B, H, N, d) (query rows).
+ */
+fa_status fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                     int B, int H, int Hkv, int N, int d, float scale, int causal,
+                     fa_dtype dtype, const int32_t *kv_len, const void *o_res, void *workspace,
+                     size_t workspace_bytes, void *stream);
 
 /* Block-sparse backward: fa_bwd with the block mask of fa_fwd_blocksparse. */
 fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,

@@ -86,6 +86,18 @@ def test_bwd_rejects_bad_arguments():
     assert st == 1
 
 
+def test_gqa_rejects_bad_head_counts():
+    lib = fa.load_library()
+    c = ctypes.c_float(0.125)
+    for Hkv in (3, 0, 5):  # must divide H = 4 and lie in [1, H]
+        st = lib.fa_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, Hkv, 128, 64, c, 0, 0, None, None,
+                            None)
+        assert st == 1
+        st = lib.fa_bwd_gqa(*([FAKE] * 9), 1, 4, Hkv, 128, 64, c, 0, 0, None, None, FAKE, 1 << 30,
+                            None)
+        assert st == 1
+
+
 def test_blocksparse_rejects_missing_mask():
     lib = fa.load_library()
     st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
