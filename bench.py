@@ -40,10 +40,10 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources hashed in "source_sha256"; see profiles/.
 TRAFFIC = {
-    "source_sha256": "c356a8c2222679729c4edf899d0ec727c1883788d58c70e2e54fdca7e4a134ce",
+    "source_sha256": "d066ca1803a0b04c923513cfaed9a86cd3f5efdd180cd8c71b38713a3da94096",
     # measured on B/4 of each sweep point (ncu, one launch) and scaled by 4 (DRAM
     # bytes grow with the number of heads): see profiles/bwd_main_kernel_*.md
-    "bytes_per_launch": {"4096": 4 * 290137088, "8192": 4 * 373601280, "16384": 4 * 395916288},
+    "bytes_per_launch": {"4096": 4 * 290130176, "8192": 4 * 372899584, "16384": 4 * 396011776},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
@@ -457,9 +457,20 @@ def run_configs(args):
         dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         gqa = w.hkv is not None and w.hkv != w.H
         ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+        split = w.num_splits is not None
+        if split:
+            n_splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.N, w.d, w.causal, w.num_splits)
+            ws_split = torch.empty(max(1, fa.fa_fwd_splitkv_workspace_size(
+                w.B, w.H, w.N, w.d, w.causal, w.num_splits)), dtype=torch.uint8, device=dev)
+
+        def fwd_unsplit(res):
+            fa.fa_fwd_gqa(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res, stream=stream)
 
         def fwd(res):
-            if bm is not None:
+            if split:
+                fa.fa_fwd_splitkv(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res,
+                                  num_splits=w.num_splits, workspace=ws_split, stream=stream)
+            elif bm is not None:
                 fa.fa_fwd_blocksparse(q, k, v, o, lse, w.scale, bm, o_res=res, stream=stream)
             elif gqa:
                 fa.fa_fwd_gqa(q, k, v, o, lse, w.scale, w.causal, kl, o_res=res, stream=stream)
@@ -483,6 +494,10 @@ def run_configs(args):
         line.update(fwd_ms=round(ms, 4), fwd_tflops=round(ff / ms / 1e9, 1))
         ms = timed(lambda: fwd(o_res))
         line.update(fwd_res_ms=round(ms, 4), fwd_res_tflops=round(ff / ms / 1e9, 1))
+        if split:
+            ms = timed(lambda: fwd_unsplit(None))
+            line.update(num_splits=n_splits, unsplit_fwd_ms=round(ms, 4),
+                        unsplit_fwd_tflops=round(ff / ms / 1e9, 1))
         if w.backward:
             fwd(o_res)
             ms = timed(bwd)

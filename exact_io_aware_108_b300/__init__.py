@@ -21,6 +21,9 @@ from ._binding import (  # noqa: F401
     fa_fwd_blocksparse,
     fa_fwd_ex,
     fa_fwd_gqa,
+    fa_fwd_splitkv,
+    fa_fwd_splitkv_num_splits,
+    fa_fwd_splitkv_workspace_size,
     fa_get_device_error,
     fa_last_error_message,
     fa_status_str,

@@ -18,7 +18,8 @@ FA_F16, FA_BF16 = 0, 1
 
 # every symbol include/fa.h declares
 EXPORTS = (
-    "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_bwd_workspace_size", "fa_bwd",
+    "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
+    "fa_fwd_splitkv_workspace_size", "fa_bwd_workspace_size", "fa_bwd",
     "fa_bwd_gqa", "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace",
     "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
@@ -64,6 +65,12 @@ def load_library():
                                            _vp]
         lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp,
                                    _vp]
+        lib.fa_fwd_splitkv.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp,
+                                       _i, _vp, _sz, _vp]
+        lib.fa_fwd_splitkv_num_splits.argtypes = [_i, _i, _i, _i, _i, _i]
+        lib.fa_fwd_splitkv_num_splits.restype = _i
+        lib.fa_fwd_splitkv_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+        lib.fa_fwd_splitkv_workspace_size.restype = _sz
         lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_bwd_workspace_size.restype = _sz
         bwd = [_vp] * 9 + [_i, _i, _i, _i, _f]
@@ -84,7 +91,8 @@ def load_library():
         lib.fa_last_error_message.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_bwd", "fa_bwd_gqa",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_bwd",
+                     "fa_bwd_gqa",
                      "fa_bwd_blocksparse",
                      "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
             getattr(lib, name).restype = _i
@@ -166,6 +174,28 @@ def fa_fwd_gqa(q, k, v, o, lse, scale, causal=False, kv_len=None, o_res=None, st
                                      float(scale), int(bool(causal)), _dtype_code(q), _ptr(kv_len),
                                      _ptr(o_res), _stream(stream)),
            "fa_fwd_gqa")
+
+
+def fa_fwd_splitkv_num_splits(B, H, N, d, causal=False, num_splits=0) -> int:
+    return int(load_library().fa_fwd_splitkv_num_splits(int(B), int(H), int(N), int(d), int(bool(causal)),
+                                                         int(num_splits)))
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, causal=False, num_splits=0) -> int:
+    return int(load_library().fa_fwd_splitkv_workspace_size(int(B), int(H), int(N), int(d),
+                                                            int(bool(causal)), int(num_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, scale, causal=False, kv_len=None, o_res=None, num_splits=0,
+                   workspace=None, workspace_bytes=None, stream=None):
+    """q, o [B, H, N, d]; k, v [B, Hkv, N, d]; num_splits <= 0 lets the library choose."""
+    B, H, N, d = _dims(q)
+    Hkv = int(k.shape[1])
+    _check(load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                         float(scale), int(bool(causal)), _dtype_code(q), _ptr(kv_len),
+                                         _ptr(o_res), int(num_splits), _ptr(workspace),
+                                         _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_fwd_splitkv")
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

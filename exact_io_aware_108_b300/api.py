@@ -9,19 +9,29 @@ from . import _binding as B
 
 
 def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None,
-                      return_residual=False, stream=None):
+                      return_residual=False, num_splits=None, stream=None):
     """O [B,H,N,d] and LSE [B,H,N] fp32 of exact attention (device tensors).
 
     k and v may have fewer heads than q (grouped-query attention: [B,Hkv,N,d]
     with H a multiple of Hkv). With return_residual=True also returns O's
     rounding residual (same dtype), which attention_backward uses for a more
-    accurate D = rowsum(dO * O)."""
+    accurate D = rowsum(dO * O). num_splits (not with block_mask) selects the
+    split-KV forward: the key tiles of each query tile shared by that many
+    CTAs (0: the library's choice)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     o_res = torch.empty_like(q) if return_residual else None
-    if block_mask is not None:
+    if num_splits is not None:
+        if block_mask is not None:
+            raise ValueError("num_splits does not combine with block_mask")
+        Bsz, H, N, d = q.shape
+        ws_bytes = B.fa_fwd_splitkv_workspace_size(Bsz, H, N, d, causal, num_splits)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+        B.fa_fwd_splitkv(q, k, v, o, lse, scale, causal, kv_len, o_res=o_res, num_splits=num_splits,
+                         workspace=ws, stream=stream)
+    elif block_mask is not None:
         B.fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, o_res=o_res, stream=stream)
     elif k.shape[1] != q.shape[1]:
         B.fa_fwd_gqa(q, k, v, o, lse, scale, causal, kv_len, o_res=o_res, stream=stream)

@@ -145,7 +145,7 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
-  kern<<<grid, 256, smem, st>>>(tq, tk, tv, a);
+  kern<<<dim3(grid, a.num_splits), 256, smem, st>>>(tq, tk, tv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
   return FA_OK;
@@ -186,10 +186,27 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   return true;
 }
 
+// Split-KV merge: one thread per 4 channels of a query row.
+template <bool BF16>
+fa_status launch_merge(const fa::FwdArgs &a, long long rows, int d, cudaStream_t st) {
+  const long long threads = rows * (d / 4);
+  const long long blocks = std::min<long long>((threads + 255) / 256, 148ll * 16);
+  fa::fwd_merge_kernel<BF16><<<static_cast<int>(blocks), 256, 0, st>>>(a, rows, d);
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? cuda_fail(e, "split-KV merge launch") : FA_OK;
+}
+
 template <int D, bool BF16, bool SPLIT>
 fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
   if (sparse) return launch_fwd_t<D, BF16, false, true, SPLIT>(tq, tk, tv, a, grid, st);
+  if (a.num_splits > 1) {
+    // split-KV: single-tile kernel over (query tile, split), then the merge
+    const fa_status r = causal ? launch_fwd_t<D, BF16, true, false, SPLIT>(tq, tk, tv, a, grid, st)
+                               : launch_fwd_t<D, BF16, false, false, SPLIT>(tq, tk, tv, a, grid, st);
+    if (r != FA_OK) return r;
+    return launch_merge<BF16>(a, static_cast<long long>(grid / a.nqt) * a.N, D, st);
+  }
   // dense / causal / key padding: two query tiles per CTA
   const long long bh = grid / a.nqt;
   const int grid2 = static_cast<int>(bh * ((a.nqt + 1) / 2));
@@ -220,13 +237,68 @@ fa_status check_kv_heads(int H, int *Hkv, bool sparse) {
   return FA_OK;
 }
 
+// SMs of the current device (148 on B300; that figure when the query fails).
+int sm_count() {
+  static std::mutex mu;
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (n[dev] == 0) {
+    int v = 0;
+    n[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
+  }
+  return n[dev];
+}
+
+constexpr int kMaxSplits = 256;
+
+// Split-KV factor: the request when it is >= 1, else the S in [1, min(64,
+// key tiles)] that minimises the modelled time ceil(ctas * S / SMs) waves of
+// (ceil(T / S) + 1) tile times each (T = key tiles of an average row; the
+// +1 stands for the CTA's prologue, epilogue and its share of the merge);
+// ties go to the smaller S.
+int resolve_splits(long long ctas, int nkt, bool causal, int requested) {
+  if (requested >= 1) return requested;
+  const int T = causal ? (nkt + 1) / 2 : nkt;
+  const long long sms = sm_count();
+  int best = 1;
+  double best_cost = 0.0;
+  for (int S = 1; S <= std::min(64, std::max(1, T)); ++S) {
+    const double waves = static_cast<double>((ctas * S + sms - 1) / sms);
+    const double cost = waves * (static_cast<double>((T + S - 1) / S) + 1.0);
+    if (S == 1 || cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Split-KV workspace: fp32 O / l [S][R][d] then fp32 LSE [S][R], R = B*H*nqt*128.
+size_t splitkv_ws_bytes(long long BH, int nqt, int d, int S) {
+  if (S <= 1) return 0;
+  const size_t R = static_cast<size_t>(BH) * nqt * 128;
+  return static_cast<size_t>(S) * R * (static_cast<size_t>(d) + 1) * 4;
+}
+
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int N, int d, float scale, int causal, fa_dtype dt, const int32_t *kv_len,
-                   const uint8_t *block_mask, bool sparse, void *o_res, void *stream, int Hkv = 0) {
+                   const uint8_t *block_mask, bool sparse, void *o_res, void *stream, int Hkv = 0,
+                   int num_splits = 1, void *workspace = nullptr, size_t ws_bytes = 0) {
   Shape s;
   fa_status r = check_common(B, H, N, d, scale, dt, &s);
   if (r != FA_OK) return r;
   if ((r = check_kv_heads(H, &Hkv, sparse)) != FA_OK) return r;
+  if (num_splits > kMaxSplits) return fail(FA_ERR_INVALID_ARG, "num_splits=%d exceeds %d", num_splits, kMaxSplits);
+  const int S = resolve_splits(s.BH * s.nqt, s.nqt, causal != 0, num_splits);
+  if (S > 1) {
+    const size_t need = splitkv_ws_bytes(s.BH, s.nqt, d, S);
+    if (workspace == nullptr) return fail(FA_ERR_INVALID_ARG, "workspace is null (num_splits=%d)", S);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(FA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    if (ws_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  }
   const long long BHkv = static_cast<long long>(B) * Hkv;
   r = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
   if (r != FA_OK) return r;
@@ -256,6 +328,9 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.hgroup = head_group(N, d, causal != 0);
   a.Hkv = Hkv;
   a.kv_group = H / Hkv;
+  a.num_splits = S;
+  a.o_part = S > 1 ? static_cast<float *>(workspace) : nullptr;
+  a.lse_part = S > 1 ? a.o_part + static_cast<size_t>(S) * s.BH * s.nqt * 128 * d : nullptr;
   a.scale_log2 = scale * 1.4426950408889634f;
   const int grid = static_cast<int>(s.BH * s.nqt);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -490,6 +565,27 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
   if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
                   o_res, stream, Hkv);
+}
+
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits > kMaxSplits) return 0;
+  const int nqt = (N + 127) / 128;
+  return resolve_splits(static_cast<long long>(B) * H * nqt, nqt, causal != 0, num_splits);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int causal, int num_splits) {
+  const int S = fa_fwd_splitkv_num_splits(B, H, N, d, causal, num_splits);
+  if (S < 1) return 0;
+  return splitkv_ws_bytes(static_cast<long long>(B) * H, (N + 127) / 128, d, S);
+}
+
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int H, int Hkv, int N, int d, float scale, int causal, fa_dtype dtype,
+                         const int32_t *kv_len, void *o_res, int num_splits, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
+                  o_res, stream, Hkv, num_splits, workspace, workspace_bytes);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

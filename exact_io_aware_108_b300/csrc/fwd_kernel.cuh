@@ -47,6 +47,13 @@ struct FwdArgs {
   int hgroup;    // heads per scheduling group of the two-tile kernel's causal launch order
   int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
   int kv_group;  // query heads per key/value head
+  // split-KV (single-tile kernel only): grid.y = num_splits CTAs share the
+  // key tiles of a query tile; each writes O / l (fp32) of its share into
+  // o_part [num_splits][BH*nqt*128][D] and its LSE into lse_part
+  // [num_splits][BH*nqt*128]; fwd_merge_kernel combines them.
+  int num_splits;
+  float *o_part;
+  float *lse_part;
   float scale_log2;
   // [B*Hkv] index of the key/value head that query head bh ([B*H] index) reads
   __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
@@ -160,8 +167,11 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int n_tiles = SPARSE ? static_cast<int>(misc[2])
-                             : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
+  const int n_all = SPARSE ? static_cast<int>(misc[2]) : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
+  // split-KV: this CTA's contiguous share [t_lo, t_lo + n_tiles) of the tiles
+  const int split = static_cast<int>(blockIdx.y);
+  const int t_lo = static_cast<int>(static_cast<long long>(n_all) * split / a.num_splits);
+  const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (split + 1) / a.num_splits) - t_lo;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -176,7 +186,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % C::kStages;
         const uint32_t ph = (t / C::kStages) & 1;
-        const int kt = SPARSE ? list[t] : t;
+        const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
         if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int sb = t & 1;
-      const int kt = SPARSE ? list[t] : t;
+      const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
       if (!mbar_wait_warp(bar(C::kBSF + sb), (t >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[128];
@@ -344,6 +354,7 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_after();
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    const float lse_row = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     uint16_t *orow = static_cast<uint16_t *>(a.o) +
                      (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
     uint32_t oall[D / 32][32];
@@ -359,6 +370,20 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) oall[j][i] = 0u;
     }
+    if (a.num_splits > 1) {
+      // split-KV partial: O / l in fp32 and this share's LSE (rows past N
+      // included: the merge reads only rows < N)
+      const size_t prow = static_cast<size_t>(split) * a.nqt * 128 * (gridDim.x / a.nqt) +
+                          static_cast<size_t>(bh) * a.nqt * 128 + static_cast<size_t>(q_row);
+      float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * D);
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          dst[(32 * j + i) / 4] = make_float4(__uint_as_float(oall[j][i]) * inv_l, __uint_as_float(oall[j][i + 1]) * inv_l,
+                                              __uint_as_float(oall[j][i + 2]) * inv_l, __uint_as_float(oall[j][i + 3]) * inv_l);
+      a.lse_part[prow] = lse_row;
+    } else {
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       const uint32_t (&o)[32] = oall[c0 / 32];
@@ -383,9 +408,8 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
-    if (q_row < a.N)
-      a.lse[static_cast<size_t>(bh) * a.N + q_row] =
-          (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    if (q_row < a.N) a.lse[static_cast<size_t>(bh) * a.N + q_row] = lse_row;
+    }
   }
 
   tc_fence_before();
@@ -394,6 +418,56 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------- split-KV merge
+// Combines the num_splits partial results of each query row with the softmax
+// merge identity ("Flash Attention: revolutionizing transformer efficiency",
+// section "The Math Behind Flash Attention": for the scores split x u y,
+// LSE(x u y) = log(e^LSE(x) + e^LSE(y)) and softmax(x u y) V is the
+// e^(LSE(part) - LSE) weighted sum of the parts' results):
+//   M = max_s LSE_s, w_s = e^(LSE_s - M), LSE = M + log sum_s w_s,
+//   O = sum_s w_s O_s / sum_s w_s.
+// A row whose parts all have LSE = -inf (no key) gets O = 0, LSE = -inf.
+// One thread per 4 channels of a row.
+template <bool BF16>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a, long long rows, int D) {
+  const long long per_row = D / 4;
+  const long long tile_rows = static_cast<long long>(a.nqt) * 128;
+  const long long part_rows = tile_rows * (rows / a.N);  // BH * nqt * 128
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < rows * per_row;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = g / per_row, c = (g % per_row) * 4;
+    const long long bh = row / a.N, i = row % a.N;
+    const long long prow = bh * tile_rows + i;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < a.num_splits; ++sp) mx = fmaxf(mx, a.lse_part[sp * part_rows + prow]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int sp = 0; sp < a.num_splits; ++sp) {
+        const float ls = a.lse_part[sp * part_rows + prow];
+        if (ls == -INFINITY) continue;
+        const float w = expf(ls - mx);
+        const float4 o = *reinterpret_cast<const float4 *>(a.o_part + (sp * part_rows + prow) * D + c);
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+        wsum += w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float x[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+    uint2 pk, rk;
+    pk.x = pack2<BF16>(x[0], x[1]);
+    pk.y = pack2<BF16>(x[2], x[3]);
+    rk.x = pack2<BF16>(x[0] - unpack_lo<BF16>(pk.x), x[1] - unpack_hi<BF16>(pk.x));
+    rk.y = pack2<BF16>(x[2] - unpack_lo<BF16>(pk.y), x[3] - unpack_hi<BF16>(pk.y));
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.o) + row * D + c) = pk;
+    if (a.o_res != nullptr) *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.o_res) + row * D + c) = rk;
+    if (c == 0) a.lse[row] = (mx == -INFINITY) ? -INFINITY : mx + logf(wsum);
   }
 }
 

@@ -41,6 +41,7 @@ class Workload:
     seed: int = 0
     backward: bool = True
     hkv: int | None = None            # key/value heads (grouped-query attention), None = H
+    num_splits: int | None = None     # split-KV forward (0 = the library's choice), None = off
     notes: str = field(default="", compare=False)
 
     @property
@@ -72,6 +73,10 @@ WORKLOADS = {
     # grouped-query attention (32 query heads sharing 8 key/value heads)
     "gqa_b4_h32_hkv8_n4096_d128_bf16_causal": Workload(
         "gqa_b4_h32_hkv8_n4096_d128_bf16_causal", 4, 32, 4096, 128, "bf16", causal=True, hkv=8),
+    # one long head: 64 query tiles cannot fill 148 SMs without splitting the keys
+    "splitkv_b1_h1_n8192_d128_bf16": Workload(
+        "splitkv_b1_h1_n8192_d128_bf16", 1, 1, 8192, 128, "bf16", qk_mult=2.0, backward=False,
+        num_splits=0),
 }
 
 

@@ -131,6 +131,47 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
                      fa_dtype dtype, const int32_t *kv_len, void *o_res, void *stream);
 
 /*
+ * Split-KV forward: the key tiles of every 128-row query tile are divided
+ * into S contiguous shares, one CTA per (query tile, share), so that few
+ * heads still fill the GPU. Each CTA writes its share's normalised fp32
+ * O_s = (sum over its keys of p V) / l_s and LSE_s; a second kernel combines
+ * the shares with the softmax merge identity ("Flash Attention:
+ * revolutionizing transformer efficiency", section "The Math Behind Flash
+ * Attention", softmax merger):
+ *   LSE = M + log sum_s e^(LSE_s - M),  O = sum_s e^(LSE_s - LSE) O_s,
+ *   M = max_s LSE_s; shares without keys (LSE_s = -inf) contribute nothing.
+ * O, lse, o_res mean what they mean for fa_fwd_gqa (same layouts, q, k, v as
+ * there); the result equals fa_fwd_gqa's up to fp32 rounding order.
+ *   num_splits: S >= 1 as given (S may exceed the key tiles of a row; the
+ *     surplus shares are empty); <= 0 lets the library choose S from the
+ *     grid size and the SM count (fa_fwd_splitkv_num_splits). At most 256.
+ *     S == 1 runs fa_fwd_gqa itself and needs no workspace.
+ *   workspace: DEVICE memory of at least
+ *     fa_fwd_splitkv_workspace_size(B, H, N, d, causal, num_splits) bytes,
+ *     256-byte aligned, owned by the caller, contents ignored on entry; may
+ *     be NULL when that size is 0.
+ * Invalid sizes, pointers or a short workspace: FA_ERR_INVALID_ARG, nothing
+ * launched.
+ */
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int H, int Hkv, int N, int d, float scale, int causal,
+                         fa_dtype dtype, const int32_t *kv_len, void *o_res, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The S fa_fwd_splitkv uses for these arguments (num_splits >= 1: itself;
+ * <= 0: the library's choice for the current device), 0 for invalid sizes.
+ */
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_splits);
+
+/*
+ * Workspace bytes of fa_fwd_splitkv: with R = B * H * ceil(N / 128) * 128
+ * padded query rows, fp32 O_s [S][R][d] then fp32 LSE_s [S][R];
+ * 0 when S == 1 or for invalid sizes.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int causal, int num_splits);
+
+/*
  * Bytes of device workspace fa_bwd / fa_bwd_blocksparse need for these
  * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
  * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ

@@ -98,6 +98,35 @@ def test_gqa_rejects_bad_head_counts():
         assert st == 1
 
 
+def test_splitkv_sizes_and_argument_checks():
+    lib = fa.load_library()
+    c = ctypes.c_float(0.125)
+    R = 1 * 2 * 8 * 128  # query rows padded to whole tiles (N = 1000)
+    assert fa.fa_fwd_splitkv_workspace_size(1, 2, 1000, 128, False, 3) == 3 * R * 129 * 4
+    assert fa.fa_fwd_splitkv_workspace_size(1, 2, 1000, 128, False, 1) == 0
+    assert fa.fa_fwd_splitkv_num_splits(1, 2, 1000, 128, False, 5) == 5
+    assert fa.fa_fwd_splitkv_num_splits(1, 2, 1000, 96, False, 5) == 0
+    assert fa.fa_fwd_splitkv_num_splits(1, 2, 1000, 128, False, 257) == 0
+    # the library's choice: >= 2 shares when one head cannot fill the SMs,
+    # none for a grid of thousands of CTAs, never more than the key tiles
+    for causal in (False, True):
+        s = fa.fa_fwd_splitkv_num_splits(1, 1, 8192, 128, causal, 0)
+        assert 2 <= s <= 64
+        assert fa.fa_fwd_splitkv_num_splits(16, 16, 4096, 128, causal, 0) == 1
+    assert fa.fa_fwd_splitkv_num_splits(1, 1, 200, 64, False, 0) <= 2
+
+    def call(num_splits, ws, ws_bytes, Hkv=2):
+        return lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, Hkv, 1000, 128, c, 0, 1, None,
+                                  None, num_splits, ws, ws_bytes, None)
+    need = 4 * R * 129 * 4
+    assert call(4, None, need) == 1             # workspace missing
+    assert call(4, FAKE + 16, need) == 1        # not 256-byte aligned
+    assert call(4, FAKE, need - 4) == 1         # too small
+    assert call(300, FAKE, 1 << 40) == 1        # more than 256 shares
+    assert call(4, FAKE, need, Hkv=3) == 1      # Hkv must divide H
+    assert call(4, FAKE, need, Hkv=0) == 1
+
+
 def test_blocksparse_rejects_missing_mask():
     lib = fa.load_library()
     st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
