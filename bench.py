@@ -447,6 +447,27 @@ def run_configs(args):
         return e0.elapsed_time(e1) / args.steps
 
     for name, w in inputs.WORKLOADS.items():
+        if w.dtype == "e4m3":
+            # 8-bit q, k, v: forward only, against the fp8 tensor rate (the
+            # measured bf16 burst x 2, the nominal fp8 / bf16 ratio)
+            t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inputs.make_workload(w).items()}
+            o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device=dev)
+            hkv = w.hkv or w.H
+            ws8 = torch.empty(fa.fa_fwd_fp8_workspace_size(w.B, hkv, w.N, w.d), dtype=torch.uint8, device=dev)
+            kl = t["kv_len"].to(torch.int32) if "kv_len" in t else None
+
+            def fwd8():
+                fa.fa_fwd_fp8(t["q"], t["k"], t["v"], o, lse, w.scale, t["q_descale"], t["k_descale"],
+                              t["v_descale"], w.causal, kl, workspace=ws8, stream=stream)
+            ff = flops_fwd(w)
+            ms = timed(fwd8)
+            line = {"config": name, "density": 1.0, "fwd_gflop": round(ff / 1e9, 3), "fwd_ms": round(ms, 4),
+                    "fwd_tflops": round(ff / ms / 1e9, 1),
+                    "fwd_frac_of_fp8_peak": round(ff / ms / 1e9 / (2 * peaks["bf16_tflops"]), 4),
+                    "fp8_peak_tflops": 2 * peaks["bf16_tflops"]}
+            print(json.dumps(line), flush=True)
+            continue
         t = {k: v.to(dev) for k, v in inputs.make_workload(w, with_dout=True).items()}
         q, k, v, dout = t["q"], t["k"], t["v"], t["dout"]
         kl = t["kv_len"].to(torch.int32) if "kv_len" in t else None

@@ -20,6 +20,8 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_blocksparse,
     fa_fwd_ex,
+    fa_fwd_fp8,
+    fa_fwd_fp8_workspace_size,
     fa_fwd_gqa,
     fa_fwd_splitkv,
     fa_fwd_splitkv_num_splits,
@@ -32,4 +34,4 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
 )
-from .api import attention_backward, attention_forward  # noqa: F401
+from .api import attention_backward, attention_forward, attention_forward_fp8  # noqa: F401

@@ -19,7 +19,8 @@ FA_F16, FA_BF16 = 0, 1
 # every symbol include/fa.h declares
 EXPORTS = (
     "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
-    "fa_fwd_splitkv_workspace_size", "fa_bwd_workspace_size", "fa_bwd",
+    "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_bwd_workspace_size",
+    "fa_bwd",
     "fa_bwd_gqa", "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace",
     "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
@@ -71,6 +72,10 @@ def load_library():
         lib.fa_fwd_splitkv_num_splits.restype = _i
         lib.fa_fwd_splitkv_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
         lib.fa_fwd_splitkv_workspace_size.restype = _sz
+        lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _f, _f, _f, _vp, _vp,
+                                   _sz, _vp]
+        lib.fa_fwd_fp8_workspace_size.argtypes = [_i, _i, _i, _i]
+        lib.fa_fwd_fp8_workspace_size.restype = _sz
         lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_bwd_workspace_size.restype = _sz
         bwd = [_vp] * 9 + [_i, _i, _i, _i, _f]
@@ -91,7 +96,8 @@ def load_library():
         lib.fa_last_error_message.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_bwd",
+        for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_fp8",
+                     "fa_bwd",
                      "fa_bwd_gqa",
                      "fa_bwd_blocksparse",
                      "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
@@ -196,6 +202,23 @@ def fa_fwd_splitkv(q, k, v, o, lse, scale, causal=False, kv_len=None, o_res=None
                                          _ptr(o_res), int(num_splits), _ptr(workspace),
                                          _ws_bytes(workspace, workspace_bytes), _stream(stream)),
            "fa_fwd_splitkv")
+
+
+def fa_fwd_fp8_workspace_size(B, Hkv, N, d) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_size(int(B), int(Hkv), int(N), int(d)))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, scale, q_descale, k_descale, v_descale, causal=False, kv_len=None,
+               workspace=None, workspace_bytes=None, stream=None):
+    """q [B, H, N, d], k, v [B, Hkv, N, d] as float8_e4m3fn (real values = descale x stored);
+    o [B, H, N, d] bf16; lse [B, H, N] fp32."""
+    B, H, N, d = _dims(q)
+    Hkv = int(k.shape[1])
+    _check(load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                     float(scale), int(bool(causal)), float(q_descale), float(k_descale),
+                                     float(v_descale), _ptr(kv_len), _ptr(workspace),
+                                     _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_fwd_fp8")
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

@@ -42,6 +42,23 @@ def attention_forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask
     return (o, lse, o_res) if return_residual else (o, lse)
 
 
+def attention_forward_fp8(q, k, v, q_descale, k_descale, v_descale, scale=None, causal=False,
+                          kv_len=None, stream=None):
+    """O [B,H,N,d] bf16 and LSE [B,H,N] fp32 of exact attention on 8-bit
+    inputs: q [B,H,N,128], k, v [B,Hkv,N,128] torch.float8_e4m3fn device
+    tensors whose real values are descale x stored (per-tensor factors)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    Bsz, H, N, d = q.shape
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(1, B.fa_fwd_fp8_workspace_size(Bsz, k.shape[1], N, d)), dtype=torch.uint8,
+                     device=q.device)
+    B.fa_fwd_fp8(q, k, v, o, lse, scale, q_descale, k_descale, v_descale, causal, kv_len,
+                 workspace=ws, stream=stream)
+    return o, lse
+
+
 def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=None,
                        block_mask=None, o_res=None, workspace=None, stream=None):
     """dQ, dK, dV of exact attention (device tensors); dK and dV have k's shape

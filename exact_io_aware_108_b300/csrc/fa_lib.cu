@@ -17,6 +17,7 @@
 #include "fa.h"
 #include "fwd_kernel.cuh"
 #include "fwd2_kernel.cuh"
+#include "fwd_fp8.cuh"
 #include "bwd_kernel.cuh"
 
 namespace {
@@ -73,6 +74,27 @@ fa_status make_tile_map(CUtensorMap *m, const void *ptr, fa_dtype dt, int N, lon
                   3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return FA_OK;
+}
+
+// 8-bit tensor [rows_outer, rows, inner] (inner bytes contiguous, row pitch
+// `pitch` bytes, a multiple of 16) as a 3-D TMA map with 128 x 128 x 1 boxes
+// (128 bytes wide), 128-byte swizzle. Elements past `inner` or `rows` read
+// as zero.
+fa_status make_tile_map8(CUtensorMap *m, const void *ptr, long long inner, long long pitch, int rows,
+                         long long outer, const char *name) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch),
+                           static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
   return FA_OK;
 }
@@ -155,10 +177,11 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 // warpgroups, which is only safe when the kernel was built with exactly the
 // register count the split assumes (checked once per kernel and device).
 // Returns false (nothing launched) when that check fails.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
 bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                      const fa::FwdArgs &a, int nqb_grid, cudaStream_t st, fa_status *r) {
-  auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, SPLIT>;
+  auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, SPLIT, FP8>;
+  using C2 = fa::Fwd2Cfg<D, FP8>;
   static std::mutex mu;
   static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
   int dev = 0;
@@ -168,13 +191,13 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     if (usable[dev] == 0) {
       cudaFuncAttributes at;
       usable[dev] = (cudaFuncGetAttributes(&at, reinterpret_cast<const void *>(kern)) == cudaSuccess &&
-                     at.numRegs == fa::Fwd2Cfg<D>::kLaunchRegs)
+                     at.numRegs == C2::kLaunchRegs)
                         ? 1
                         : -1;
     }
     if (usable[dev] < 0) return false;
   }
-  constexpr int smem = fa::Fwd2Cfg<D>::kSmemBytes;
+  constexpr int smem = C2::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) {
     *r = cuda_fail(e, "cudaFuncSetAttribute(fwd2)");
@@ -332,6 +355,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.o_part = S > 1 ? static_cast<float *>(workspace) : nullptr;
   a.lse_part = S > 1 ? a.o_part + static_cast<size_t>(S) * s.BH * s.nqt * 128 * d : nullptr;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.o_scale = 1.f;
   const int grid = static_cast<int>(s.BH * s.nqt);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
@@ -586,6 +610,72 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
   if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, kv_len, nullptr, false,
                   o_res, stream, Hkv, num_splits, workspace, workspace_bytes);
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d) {
+  if (B < 1 || Hkv < 1 || N < 1 || d != 128) return 0;
+  const size_t npad = static_cast<size_t>((N + 127) / 128) * 128;
+  return static_cast<size_t>(B) * Hkv * d * npad;
+}
+
+fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                     int Hkv, int N, int d, float scale, int causal, float q_descale, float k_descale,
+                     float v_descale, const int32_t *kv_len, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+  Shape s;
+  fa_status r = check_common(B, H, N, d, scale, FA_BF16, &s);
+  if (r != FA_OK) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "the 8-bit forward is built for d = 128 (got %d)", d);
+  if (Hkv < 1) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must be >= 1", Hkv);
+  if ((r = check_kv_heads(H, &Hkv, false)) != FA_OK) return r;
+  for (float f : {q_descale, k_descale, v_descale})
+    if (!(f > 0.f) || !std::isfinite(f))
+      return fail(FA_ERR_INVALID_ARG, "dequantisation factors must be finite and > 0");
+  if (!std::isfinite(scale * q_descale * k_descale))
+    return fail(FA_ERR_INVALID_ARG, "scale * q_descale * k_descale overflows");
+  r = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {workspace, "workspace"}});
+  if (r != FA_OK) return r;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(FA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = fa_fwd_fp8_workspace_size(B, Hkv, N, d);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "kv_len is not 4-byte aligned");
+  const long long BHkv = static_cast<long long>(B) * Hkv;
+  const int npad = s.nqt * 128;
+  CUtensorMap tq, tk, tv;
+  if ((r = make_tile_map8(&tq, q, d, d, N, s.BH, "q")) != FA_OK) return r;
+  if ((r = make_tile_map8(&tk, k, d, d, N, BHkv, "k")) != FA_OK) return r;
+  if ((r = make_tile_map8(&tv, workspace, N, npad, d, BHkv, "v^T")) != FA_OK) return r;
+  if (BHkv > 65535) return fail(FA_ERR_UNSUPPORTED, "B*Hkv=%lld exceeds 65535", BHkv);
+  fa::FwdArgs a{};
+  a.o = o;
+  a.o_res = nullptr;
+  a.lse = lse;
+  a.kv_len = kv_len;
+  a.block_mask = nullptr;
+  a.H = H;
+  a.N = N;
+  a.nqt = s.nqt;
+  a.nkt = s.nqt;
+  a.hgroup = head_group(N, d, causal != 0) * 2;  // 8-bit K and V: half the bytes per head
+  a.Hkv = Hkv;
+  a.kv_group = H / Hkv;
+  a.num_splits = 1;
+  a.scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  a.o_scale = v_descale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  fa::fwd_fp8_vt_kernel<<<dim3(s.nqt, static_cast<unsigned>(BHkv)), 256, 0, st>>>(
+      static_cast<const uint8_t *>(v), static_cast<uint8_t *>(workspace), N, npad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
+  const int grid2 = static_cast<int>(s.BH * ((s.nqt + 1) / 2));
+  const bool launched = causal ? try_launch_fwd2<128, true, true, false, true>(tq, tk, tv, a, grid2, st, &r)
+                               : try_launch_fwd2<128, true, false, false, true>(tq, tk, tv, a, grid2, st, &r);
+  if (!launched) return fail(FA_ERR_CUDA, "8-bit forward: kernel register count differs from its warpgroup split");
+  if (r != FA_OK) return r;
+  return ok();
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

@@ -24,17 +24,30 @@
 //
 // Online softmax: softmax_row (softmax_row.cuh), the same arithmetic as
 // fwd_kernel.cuh.
+//
+// FP8 (d = 128 only): Q, K and V are e4m3 with per-tensor dequantisation
+// factors (low-precision forward of the FlashAttention-3 section of "Flash
+// Attention: revolutionizing transformer efficiency"). Both products run as
+// kind::f8f6f4 (K = 32 per instruction): S = Q K^T with K-major Q and K, and
+// O += P V^T-fed, where V arrives already transposed ([d][keys], written by
+// fwd_fp8_vt_kernel) so that its tile is K-major too. P is scaled by 2^8
+// before it is rounded to e4m3 (p' = 2^(x - m + 8) <= 256 < 448, and small
+// probabilities keep their mantissa down to 2^-14 instead of 2^-6); l sums
+// the unrounded p', so O = (P' V) / l' needs no correction and
+// LSE = (m + log2 l' - 8) ln 2. P takes 32 TMEM columns, four keys per column.
 #pragma once
 #include "common.cuh"
 #include "fwd_kernel.cuh"
 
 namespace fa {
 
-template <int D>
+template <int D, bool FP8 = false>
 struct Fwd2Cfg {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kKB = D / 64;
+  static_assert(!FP8 || D == 128, "the 8-bit forward is built for d = 128");
+  static constexpr int kTileBytes = 128 * D * (FP8 ? 1 : 2);
+  static constexpr int kStages = FP8 ? 4 : ((D == 64) ? 3 : 2);
+  static constexpr int kKB = FP8 ? 1 : D / 64;   // 128-byte TMA boxes per tile row
+  static constexpr int kBoxElems = FP8 ? 128 : 64;
   static constexpr int kQOff = 0;                          // Q_A, Q_B
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -62,11 +75,12 @@ struct Fwd2Cfg {
   static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kLaunchRegs * 384, "register split");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using C = Fwd2Cfg<D>;
+  static_assert(!FP8 || (BF16 && !SPLIT), "8-bit inputs give bf16 O, without residual");
+  using C = Fwd2Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw2[];
   const uint32_t raw = smem_u32(smem_raw2);
   const uint32_t sbase = align_up_1024(raw);
@@ -150,7 +164,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int x = 0; x < (has_b ? 2 : 1); ++x)
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kQOff + x * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQ),
-                           kb * 64, (2 * qb + x) * 128, bh, pol_q);
+                           kb * C::kBoxElems, (2 * qb + x) * 128, bh, pol_q);
       int nk = 0, nv = 0;
       for (int t = 0; t < n_max; ++t) {
         const int st = t % C::kStages;
@@ -159,13 +173,17 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
           tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
-                           bar(C::kBKF + st), kb * 64, t * 128, kvh, pol_kv);
+                           bar(C::kBKF + st), kb * C::kBoxElems, t * 128, kvh, pol_kv);
         nk = t + 1;
         if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
-        for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
-                           bar(C::kBVF + st), kb * 64, t * 128, kvh, pol_kv);
+        if constexpr (FP8)  // V^T: 128 keys (x) of all 128 rows d
+          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes, &tm_v, bar(C::kBVF + st), t * 128, 0,
+                           kvh, pol_kv);
+        else
+          for (int kb = 0; kb < C::kKB; ++kb)
+            tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
+                             bar(C::kBVF + st), kb * 64, t * 128, kvh, pol_kv);
         nv = t + 1;
       }
       if (*abort_flag) {
@@ -179,18 +197,27 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_max > 0) {
-      constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
-      constexpr uint32_t kIdPV = idesc_f16(BF16, 128, D, false, true);
+      // (for 8-bit inputs the e4m3 format code is f16's, 0: the same descriptor)
+      constexpr uint32_t kIdQK = idesc_f16(BF16 && !FP8, 128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_f16(BF16 && !FP8, 128, D, false, !FP8);
       // S_x(t) = Q_x K_t^T into TMEM; the caller has waited for K_t
       auto issue_qk = [&](int x, int t) {
         const uint32_t sb = opaque_u32(sbase);
         const uint32_t kbase = sb + C::kKOff + (t % C::kStages) * C::kTileBytes;
         const uint32_t qbase = sb + C::kQOff + x * C::kTileBytes;
+        if constexpr (FP8) {
+          // 32 e4m3 elements = 32 B of the single 128-byte column block per step
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 32; ++ks)
+            mma_ss_f8(tmem + C::col_s(x), sdesc_sw128(qbase + ks * 32, 16, 1024),
+                      sdesc_sw128(kbase + ks * 32, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
+                   sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          }
         }
         mma_commit(bar(C::kBSF + x));
       };
@@ -222,14 +249,23 @@ __global__ void __launch_bounds__(384, 1)
           for (int h = 0; h < 2; ++h) {
             if (!mbar_wait(bar(C::kBPF + 2 * x + h), t & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
+            if constexpr (FP8) {
+              // A = P (4 keys per TMEM column, 8 columns per step); B = V^T
+              // K-major, 32 keys = 32 B per step
 #pragma unroll
-            for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-              mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
-                     (t > 0 || ks > 0) ? 1u : 0u);
-            if constexpr (SPLIT) {
+              for (int ks = 2 * h; ks < 2 * h + 2; ++ks)
+                mma_ts_f8(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 32, 16, 1024), kIdPV,
+                          (t > 0 || ks > 0) ? 1u : 0u);
+            } else {
 #pragma unroll
               for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-                mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
+                mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
+                       (t > 0 || ks > 0) ? 1u : 0u);
+              if constexpr (SPLIT) {
+#pragma unroll
+                for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+                  mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
+              }
             }
           }
           if (!ok) break;
@@ -315,24 +351,41 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      softmax_exp<0, 64>(s, sl2, nm, acc);
+      // 8-bit P: exponent offset +8 (p' = 2^8 p), keys 4c..4c+3 in column c
+      const float nmx = FP8 ? nm + 8.f : nm;
+      softmax_exp<0, 64>(s, sl2, nmx, acc);
+      if constexpr (FP8) {
+        uint32_t w[16];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t hi[16], lo[16];
-        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
-        tmem_st_32x32b_x16(scol + c0 / 2, hi);
-        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
+        for (int i = 0; i < 16; ++i) w[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+        tmem_st_32x32b_x16(scol, w);
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t hi[16], lo[16];
+          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          tmem_st_32x32b_x16(scol + c0 / 2, hi);
+          if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBPF + 2 * x));
-      softmax_exp<64, 128>(s, sl2, nm, acc);
+      softmax_exp<64, 128>(s, sl2, nmx, acc);
+      if constexpr (FP8) {
+        uint32_t w[16];
 #pragma unroll
-      for (int c0 = 64; c0 < 128; c0 += 32) {
-        uint32_t hi[16], lo[16];
-        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
-        tmem_st_32x32b_x16(scol + c0 / 2, hi);
-        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_e4m3x4(s[64 + 4 * i], s[64 + 4 * i + 1], s[64 + 4 * i + 2], s[64 + 4 * i + 3]);
+        tmem_st_32x32b_x16(scol + 16, w);
+      } else {
+#pragma unroll
+        for (int c0 = 64; c0 < 128; c0 += 32) {
+          uint32_t hi[16], lo[16];
+          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          tmem_st_32x32b_x16(scol + c0 / 2, hi);
+          if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -347,7 +400,8 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
     }
     if (qt < a.nqt) {
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // 8-bit inputs: O carries V's dequantisation factor
+      const float inv_l = (l > 0.f) ? (FP8 ? a.o_scale : 1.f) / l : 0.f;
       uint16_t *orow = static_cast<uint16_t *>(a.o) +
                        (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
       uint32_t oall[D / 32][32];
@@ -389,7 +443,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (q_row < a.N)
         a.lse[static_cast<size_t>(bh) * a.N + q_row] =
-            (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            (l > 0.f) ? (m + log2f(l) - (FP8 ? 8.f : 0.f)) * 0.69314718055994530942f : -INFINITY;
     }
     // teardown of the softmax warpgroups
     tc_fence_before();

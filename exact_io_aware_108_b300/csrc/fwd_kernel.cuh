@@ -55,6 +55,8 @@ struct FwdArgs {
   float *o_part;
   float *lse_part;
   float scale_log2;
+  float o_scale;  // 8-bit forward: V's dequantisation factor, applied to O
+
   // [B*Hkv] index of the key/value head that query head bh ([B*H] index) reads
   __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
 };

@@ -13,7 +13,12 @@ Recipe (the pages name BERT-large seq 512, GPT-2 seq 1K, Long-Range-Arena
   * key-padding lengths ``torch.randint(lo, hi + 1, (B,))`` from the same
     generator, drawn after dO;
   * block mask ``torch.rand(nb, nb) < p`` from its own generator
-    (``manual_seed(mask_seed)``), diagonal forced to keep.
+    (``manual_seed(mask_seed)``), diagonal forced to keep;
+  * 8-bit inputs: q, k, v drawn as above in fp32, each divided by its own
+    power-of-two factor 2^ceil(log2(max|x| / 448)) and cast to
+    ``torch.float8_e4m3fn`` (round to nearest even; no value reaches the
+    448 limit); the factor is returned as the tensor's dequantisation
+    factor, and ``dequant`` gives the exact real values (fp64).
 """
 from __future__ import annotations
 
@@ -32,7 +37,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str            # "f16" | "bf16"
+    dtype: str            # "f16" | "bf16" | "e4m3" (8-bit q, k, v; bf16 O)
     causal: bool = False
     kv_len_range: tuple | None = None   # (lo, hi) inclusive
     block_sparse_p: float | None = None
@@ -50,6 +55,8 @@ class Workload:
 
     @property
     def torch_dtype(self):
+        if self.dtype == "e4m3":
+            return torch.float8_e4m3fn
         return torch.float16 if self.dtype == "f16" else torch.bfloat16
 
 
@@ -73,6 +80,9 @@ WORKLOADS = {
     # grouped-query attention (32 query heads sharing 8 key/value heads)
     "gqa_b4_h32_hkv8_n4096_d128_bf16_causal": Workload(
         "gqa_b4_h32_hkv8_n4096_d128_bf16_causal", 4, 32, 4096, 128, "bf16", causal=True, hkv=8),
+    # the N = 8192 long-context point with 8-bit q, k, v
+    "fp8_b4_h16_n8192_d128_e4m3_causal": Workload(
+        "fp8_b4_h16_n8192_d128_e4m3_causal", 4, 16, 8192, 128, "e4m3", causal=True, backward=False),
     # one long head: 64 query tiles cannot fill 148 SMs without splitting the keys
     "splitkv_b1_h1_n8192_d128_bf16": Workload(
         "splitkv_b1_h1_n8192_d128_bf16", 1, 1, 8192, 128, "bf16", qk_mult=2.0, backward=False,
@@ -113,10 +123,39 @@ def make_block_mask(N, p, seed=7, block=BLOCK):
     return m.to(torch.uint8)
 
 
+def _to_e4m3(x):
+    amax = float(x.abs().max())
+    e = math.ceil(math.log2(amax / 448.0)) if amax > 0 else 0
+    descale = 2.0 ** e
+    q8 = (x / descale).to(torch.float8_e4m3fn)
+    return q8, descale
+
+
+def make_qkv_fp8(B, H, N, d, seed=0, hkv=None, kv_len_range=None):
+    """8-bit q, k, v (float8_e4m3fn) and their dequantisation factors
+    q_descale, k_descale, v_descale (powers of two)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    kv_shape = (B, H if hkv is None else hkv, N, d)
+    out = {}
+    for name, shape in (("q", (B, H, N, d)), ("k", kv_shape), ("v", kv_shape)):
+        out[name], out[name + "_descale"] = _to_e4m3(torch.randn(shape, generator=g, dtype=torch.float32))
+    if kv_len_range is not None:
+        lo, hi = kv_len_range
+        out["kv_len"] = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return out
+
+
+def dequant(x8, descale):
+    """Real values of an e4m3 tensor (exact in fp64)."""
+    return x8.to(torch.float64) * descale
+
+
 def make_workload(w: Workload, with_dout=None):
     """All inputs of a named workload (CPU tensors)."""
     if with_dout is None:
         with_dout = w.backward
+    if w.dtype == "e4m3":
+        return make_qkv_fp8(w.B, w.H, w.N, w.d, seed=w.seed, hkv=w.hkv, kv_len_range=w.kv_len_range)
     t = make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult,
                  with_dout=with_dout, kv_len_range=w.kv_len_range, hkv=w.hkv)
     if w.block_sparse_p is not None:

@@ -7,7 +7,8 @@
  *
  * ("Flash Attention: revolutionizing transformer efficiency", standard
  * attention listing, and the FlashAttention abstract on the Tri Dao author
- * page: "an IO-aware exact attention algorithm that uses tiling"), tile by
+ * page, which describes the method as exact attention computed in tiles to
+ * save memory traffic), tile by
  * tile on the GPU with the online-softmax rescaling of the same page (section
  * "The Math Behind Flash Attention": softmax decomposition and merger), so the
  * N x N score matrix never reaches device memory. The forward pass also writes
@@ -103,8 +104,8 @@ fa_status fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float 
                     fa_dtype dtype, const int32_t *kv_len, void *o_res, void *stream);
 
 /*
- * Block-sparse forward (FlashAttention abstract: "We also extend
- * FlashAttention to block-sparse attention"). block_mask is a DEVICE uint8
+ * Block-sparse forward (the FlashAttention abstract names a block-sparse
+ * extension of the method). block_mask is a DEVICE uint8
  * array [nb, nb], nb = ceil(N / 128), row = query tile, column = key tile,
  * nonzero = keep, shared by all (b, h). Masked tiles are neither loaded nor
  * multiplied; inside a kept tile attention is dense and non-causal.
@@ -157,6 +158,35 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
                          int B, int H, int Hkv, int N, int d, float scale, int causal,
                          fa_dtype dtype, const int32_t *kv_len, void *o_res, int num_splits,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * 8-bit forward (the FlashAttention-3 section of "Flash Attention:
+ * revolutionizing transformer efficiency" names low-precision FP8 attention;
+ * the arithmetic is that of fa_fwd_gqa on the dequantised inputs):
+ *   q [B,H,N,d], k, v [B,Hkv,N,d]: DEVICE e4m3 bytes (OCP FP8 E4M3, the
+ *     layout of torch.float8_e4m3fn), 16-byte aligned; the real values are
+ *     q_descale * q, k_descale * k, v_descale * v (per-tensor factors,
+ *     finite and > 0).
+ *   o [B,H,N,d] bf16 out; lse [B,H,N] fp32 out (natural log); scale,
+ *     causal, Hkv, kv_len as in fa_fwd_gqa. d must be 128
+ *     (FA_ERR_UNSUPPORTED otherwise).
+ *   workspace: DEVICE memory of at least fa_fwd_fp8_workspace_size(B, Hkv,
+ *     N, d) bytes, 256-byte aligned, owned by the caller, contents ignored
+ *     on entry; receives V transposed per head ([d][N rounded up to 128]),
+ *     the layout the 8-bit P V product reads.
+ * Both products run on the tensor cores in e4m3 with fp32 accumulation;
+ * P = softmax probabilities times 2^8 is rounded to e4m3 (relative error
+ * <= 2^-4 per probability) before P V, the row sums use the unrounded
+ * values, so LSE is as accurate as the 16-bit forward's and O carries the
+ * rounding of P.
+ */
+fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int Hkv, int N, int d, float scale, int causal, float q_descale,
+                     float k_descale, float v_descale, const int32_t *kv_len, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of fa_fwd_fp8: B * Hkv * d * ceil(N / 128) * 128; 0 for invalid sizes. */
+size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
 
 /*
  * The S fa_fwd_splitkv uses for these arguments (num_splits >= 1: itself;

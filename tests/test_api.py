@@ -127,6 +127,24 @@ def test_splitkv_sizes_and_argument_checks():
     assert call(4, FAKE, need, Hkv=0) == 1
 
 
+def test_fp8_sizes_and_argument_checks():
+    lib = fa.load_library()
+    assert fa.fa_fwd_fp8_workspace_size(2, 3, 300, 128) == 2 * 3 * 128 * 384
+    assert fa.fa_fwd_fp8_workspace_size(2, 3, 300, 64) == 0
+    f = ctypes.c_float
+
+    def call(d=128, H=2, Hkv=2, qd=1.0, kd=1.0, vd=1.0, ws=FAKE, ws_bytes=1 << 30, q=FAKE):
+        return lib.fa_fwd_fp8(q, FAKE, FAKE, FAKE, FAKE, 1, H, Hkv, 256, d, f(0.1), 0, f(qd), f(kd), f(vd),
+                              None, ws, ws_bytes, None)
+    assert call(d=64) == 2                       # only d = 128 is built
+    assert call(qd=0.0) == 1 and call(kd=-1.0) == 1 and call(vd=float("inf")) == 1
+    assert call(ws=None) == 1                    # workspace missing
+    assert call(ws=FAKE + 64) == 1               # not 256-byte aligned
+    assert call(ws_bytes=2 * 128 * 256 - 1) == 1 # too small
+    assert call(Hkv=3) == 1 and call(Hkv=0) == 1
+    assert call(q=FAKE + 8) == 1                 # q not 16-byte aligned
+
+
 def test_blocksparse_rejects_missing_mask():
     lib = fa.load_library()
     st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
