@@ -201,3 +201,50 @@ def attn_bwd_sampled(q, k, v, dout, scale, qrows, kcols, causal=False,
     if rc != 0:
         raise ValueError("oracle_attn_bwd_sampled failed: %d" % rc)
     return dq, dk, dv, lse, delta
+
+
+def paged_decode(q, k_cache, v_cache, block_table, seq_len, scale, page_size, lib=None):
+    """Decode attention over a paged key/value cache (test infrastructure).
+
+    Page "Enhancing Transformer Models: Innovations in Attention Mechanisms
+    and Performance Optimization", section "From FlashAttention to
+    PagedAttention": the cache lives in pages. Read here as: sequence b's
+    logical page i is pool page block_table[b, i]; its first seq_len[b] keys,
+    taken page by page in logical order, are its context. The Nq new query
+    tokens are the last Nq positions of that context, so query i sits at
+    position L - Nq + i and, with the causal mask of the forward definition,
+    sees keys 0 .. L - Nq + i. Query head h reads key/value head h / (H/Hkv).
+
+    q [B,H,Nq,d]; k_cache, v_cache [num_pages, Hkv, page_size, d];
+    block_table [B, pages_per_seq]; seq_len [B]. Returns o [B,H,Nq,d] and
+    lse [B,H,Nq] (float64; a query with no visible key: 0 and -inf).
+    """
+    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    bt = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table)
+    sl = np.asarray(seq_len.cpu().numpy() if hasattr(seq_len, "cpu") else seq_len)
+    B, H, Nq, d = q.shape
+    Hkv = kc.shape[1]
+    cap = bt.shape[1] * page_size
+    o = np.zeros((B, H, Nq, d))
+    lse = np.full((B, H, Nq), -np.inf)
+    for b in range(B):
+        L = int(min(max(int(sl[b]), 0), cap))
+        if L == 0:
+            continue
+        pages = bt[b, :(L + page_size - 1) // page_size]
+        for kvh in range(Hkv):
+            keys = np.concatenate([kc[p, kvh] for p in pages], axis=0)[:L]
+            vals = np.concatenate([vc[p, kvh] for p in pages], axis=0)[:L]
+            for h in range(kvh * (H // Hkv), (kvh + 1) * (H // Hkv)):
+                pos = [L - Nq + i for i in range(Nq)]
+                live = [i for i in range(Nq) if pos[i] >= 0]
+                if not live:
+                    continue
+                qf = np.zeros((L, d))
+                for i in live:
+                    qf[pos[i]] = q[b, h, i]
+                ob, lb = attn_fwd_rows(qf, keys, vals, scale, [pos[i] for i in live], causal=True, lib=lib)
+                for n, i in enumerate(live):
+                    o[b, h, i] = ob[n]
+                    lse[b, h, i] = lb[n]
+    return o, lse
