@@ -40,10 +40,10 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources hashed in "source_sha256"; see profiles/.
 TRAFFIC = {
-    "source_sha256": "d066ca1803a0b04c923513cfaed9a86cd3f5efdd180cd8c71b38713a3da94096",
+    "source_sha256": "a4727f6d26fec2247a4aa61a0ec7b821c1f08499ba2534ded68ac2046f6143f5",
     # measured on B/4 of each sweep point (ncu, one launch) and scaled by 4 (DRAM
     # bytes grow with the number of heads): see profiles/bwd_main_kernel_*.md
-    "bytes_per_launch": {"4096": 4 * 290130176, "8192": 4 * 372899584, "16384": 4 * 396011776},
+    "bytes_per_launch": {"4096": 4 * 290788352, "8192": 4 * 375815936, "16384": 4 * 398077440},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
@@ -447,6 +447,34 @@ def run_configs(args):
         return e0.elapsed_time(e1) / args.steps
 
     for name, w in inputs.WORKLOADS.items():
+        if w.nq is not None:
+            # paged decode: HBM-bound; algorithmic bytes = the K and V rows of
+            # every sequence's context once, q and o once, lse
+            t = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inputs.make_workload(w).items()}
+            o = torch.empty_like(t["q"])
+            lse = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device=dev)
+            hkv = w.hkv or w.H
+            pps = t["block_table"].shape[1]
+            n_splits = fa.fa_decode_paged_num_splits(w.B, w.H, hkv, w.nq, w.d, w.page_size, pps, w.num_splits)
+            wsd = torch.empty(max(1, fa.fa_decode_paged_workspace_size(w.B, w.H, hkv, w.nq, w.d, w.page_size,
+                                                                       pps, w.num_splits)),
+                              dtype=torch.uint8, device=dev)
+
+            def dec():
+                fa.fa_decode_paged(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_len"], o, lse,
+                                   w.scale, num_splits=w.num_splits, workspace=wsd, stream=stream)
+            ctx = int(t["seq_len"].to(torch.int64).sum())
+            nbytes = (ctx * hkv * w.d * 2 * 2 + 2 * t["q"].numel() * 2 + lse.numel() * 4
+                      + t["block_table"].numel() * 4)
+            flops = 4.0 * ctx * w.H * w.nq * w.d
+            ms = timed(dec)
+            line = {"config": name, "num_splits": n_splits, "context_tokens": ctx,
+                    "algorithmic_bytes": nbytes, "decode_ms": round(ms, 4),
+                    "decode_gbs": round(nbytes / ms / 1e6, 1),
+                    "decode_frac_of_measured_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
+                    "decode_tflops": round(flops / ms / 1e9, 2)}
+            print(json.dumps(line), flush=True)
+            continue
         if w.dtype == "e4m3":
             # 8-bit q, k, v: forward only, against the fp8 tensor rate (the
             # measured bf16 burst x 2, the nominal fp8 / bf16 ratio)

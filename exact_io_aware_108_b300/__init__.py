@@ -17,6 +17,9 @@ from ._binding import (  # noqa: F401
     fa_bwd_noalloc_max_workspace,
     fa_bwd_prepare,
     fa_bwd_workspace_size,
+    fa_decode_paged,
+    fa_decode_paged_num_splits,
+    fa_decode_paged_workspace_size,
     fa_fwd,
     fa_fwd_blocksparse,
     fa_fwd_ex,
@@ -34,4 +37,9 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
 )
-from .api import attention_backward, attention_forward, attention_forward_fp8  # noqa: F401
+from .api import (  # noqa: F401
+    attention_backward,
+    attention_decode_paged,
+    attention_forward,
+    attention_forward_fp8,
+)

@@ -20,7 +20,7 @@ FA_F16, FA_BF16 = 0, 1
 EXPORTS = (
     "fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
     "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_bwd_workspace_size",
-    "fa_bwd",
+    "fa_decode_paged", "fa_decode_paged_num_splits", "fa_decode_paged_workspace_size", "fa_bwd",
     "fa_bwd_gqa", "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace",
     "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
@@ -76,6 +76,11 @@ def load_library():
                                    _sz, _vp]
         lib.fa_fwd_fp8_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_fwd_fp8_workspace_size.restype = _sz
+        lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp]
+        lib.fa_decode_paged_num_splits.argtypes = [_i] * 8
+        lib.fa_decode_paged_num_splits.restype = _i
+        lib.fa_decode_paged_workspace_size.argtypes = [_i] * 8
+        lib.fa_decode_paged_workspace_size.restype = _sz
         lib.fa_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
         lib.fa_bwd_workspace_size.restype = _sz
         bwd = [_vp] * 9 + [_i, _i, _i, _i, _f]
@@ -97,7 +102,7 @@ def load_library():
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_ex", "fa_fwd_blocksparse", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_fp8",
-                     "fa_bwd",
+                     "fa_decode_paged", "fa_bwd",
                      "fa_bwd_gqa",
                      "fa_bwd_blocksparse",
                      "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
@@ -219,6 +224,32 @@ def fa_fwd_fp8(q, k, v, o, lse, scale, q_descale, k_descale, v_descale, causal=F
                                      float(v_descale), _ptr(kv_len), _ptr(workspace),
                                      _ws_bytes(workspace, workspace_bytes), _stream(stream)),
            "fa_fwd_fp8")
+
+
+def fa_decode_paged_num_splits(B, H, Hkv, Nq, d, page_size, pages_per_seq, num_splits=0) -> int:
+    return int(load_library().fa_decode_paged_num_splits(int(B), int(H), int(Hkv), int(Nq), int(d),
+                                                         int(page_size), int(pages_per_seq), int(num_splits)))
+
+
+def fa_decode_paged_workspace_size(B, H, Hkv, Nq, d, page_size, pages_per_seq, num_splits=0) -> int:
+    return int(load_library().fa_decode_paged_workspace_size(int(B), int(H), int(Hkv), int(Nq), int(d),
+                                                             int(page_size), int(pages_per_seq),
+                                                             int(num_splits)))
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_table, seq_len, o, lse, scale, num_splits=0, workspace=None,
+                    workspace_bytes=None, stream=None):
+    """q, o [B, H, Nq, d]; k_cache, v_cache [num_pages, Hkv, page_size, d]; block_table int32
+    [B, pages_per_seq]; seq_len int32 [B]; lse [B, H, Nq] fp32."""
+    B, H, Nq, d = _dims(q)
+    num_pages, Hkv, page_size = (int(x) for x in k_cache.shape[:3])
+    pages_per_seq = int(block_table.shape[1])
+    _check(load_library().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                          _ptr(seq_len), _ptr(o), _ptr(lse), B, H, Hkv, Nq, d, page_size,
+                                          num_pages, pages_per_seq, float(scale), _dtype_code(q),
+                                          int(num_splits), _ptr(workspace),
+                                          _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "fa_decode_paged")
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

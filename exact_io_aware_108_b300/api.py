@@ -59,6 +59,27 @@ def attention_forward_fp8(q, k, v, q_descale, k_descale, v_descale, scale=None, 
     return o, lse
 
 
+def attention_decode_paged(q, k_cache, v_cache, block_table, seq_len, scale=None, num_splits=0,
+                           stream=None):
+    """O [B,H,Nq,d] and LSE [B,H,Nq] of the Nq newest tokens of B sequences
+    against their paged key/value cache (k_cache, v_cache [num_pages, Hkv,
+    page_size, d]; block_table int32 [B, pages_per_seq]; seq_len int32 [B]).
+    num_splits: key tiles of a sequence shared by that many CTAs (0: the
+    library's choice)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    Bsz, H, Nq, d = q.shape
+    num_pages, Hkv, page_size, _ = k_cache.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    ws_bytes = B.fa_decode_paged_workspace_size(Bsz, H, Hkv, Nq, d, page_size, block_table.shape[1],
+                                                num_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    B.fa_decode_paged(q, k_cache, v_cache, block_table, seq_len, o, lse, scale, num_splits=num_splits,
+                      workspace=ws, stream=stream)
+    return o, lse
+
+
 def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_len=None,
                        block_mask=None, o_res=None, workspace=None, stream=None):
     """dQ, dK, dV of exact attention (device tensors); dK and dV have k's shape

@@ -85,12 +85,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (tensor core) reads.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ----------------------------------------------------------------- pre
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long rows_pad) {

@@ -160,10 +160,10 @@ cudaError_t set_smem(const void *kernel, int bytes) {
   return e;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = false>
 fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
-  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT>;
+  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT, PAGED>;
   constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
@@ -352,6 +352,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.Hkv = Hkv;
   a.kv_group = H / Hkv;
   a.num_splits = S;
+  a.block_table = nullptr;
+  a.page_size = a.pages_per_seq = a.dec_nq = 0;
   a.o_part = S > 1 ? static_cast<float *>(workspace) : nullptr;
   a.lse_part = S > 1 ? a.o_part + static_cast<size_t>(S) * s.BH * s.nqt * 128 * d : nullptr;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -612,6 +614,38 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
                   o_res, stream, Hkv, num_splits, workspace, workspace_bytes);
 }
 
+// Paged decode: rows per (batch, key/value head) block and its query tiles.
+struct DecodeShape {
+  long long BHkv;
+  int R, nqt, nkt_max;
+};
+
+fa_status check_decode(int B, int H, int Hkv, int Nq, int d, int page_size, int num_pages,
+                       int pages_per_seq, float scale, fa_dtype dt, DecodeShape *s) {
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1)
+    return fail(FA_ERR_INVALID_ARG, "B, H, Hkv, Nq must be >= 1 (got %d, %d, %d, %d)", B, H, Hkv, Nq);
+  if (H % Hkv != 0 || Hkv > H) return fail(FA_ERR_INVALID_ARG, "Hkv=%d must divide H=%d", Hkv, H);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", d);
+  if (dt != FA_F16 && dt != FA_BF16) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return fail(FA_ERR_UNSUPPORTED, "page_size %d not built (16, 32, 64 or 128)", page_size);
+  if (num_pages < 1 || pages_per_seq < 1)
+    return fail(FA_ERR_INVALID_ARG, "num_pages and pages_per_seq must be >= 1");
+  if (static_cast<long long>(num_pages) * Hkv > INT_MAX / 2)
+    return fail(FA_ERR_INVALID_ARG, "num_pages * Hkv too large");
+  if (static_cast<long long>(pages_per_seq) * page_size > (1ll << 30))
+    return fail(FA_ERR_INVALID_ARG, "pages_per_seq * page_size too large");
+  const long long R = static_cast<long long>(H / Hkv) * Nq;
+  if (R > (1 << 20)) return fail(FA_ERR_INVALID_ARG, "(H / Hkv) * Nq too large");
+  s->BHkv = static_cast<long long>(B) * Hkv;
+  s->R = static_cast<int>(R);
+  s->nqt = static_cast<int>((R + 127) / 128);
+  s->nkt_max = static_cast<int>((static_cast<long long>(pages_per_seq) * page_size + 127) / 128);
+  if (s->BHkv * s->nqt > INT_MAX) return fail(FA_ERR_INVALID_ARG, "grid too large");
+  return FA_OK;
+}
+
 size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d) {
   if (B < 1 || Hkv < 1 || N < 1 || d != 128) return 0;
   const size_t npad = static_cast<size_t>((N + 127) / 128) * 128;
@@ -675,6 +709,94 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float
                                : try_launch_fwd2<128, true, false, false, true>(tq, tk, tv, a, grid2, st, &r);
   if (!launched) return fail(FA_ERR_CUDA, "8-bit forward: kernel register count differs from its warpgroup split");
   if (r != FA_OK) return r;
+  return ok();
+}
+
+int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_size,
+                               int pages_per_seq, int num_splits) {
+  DecodeShape s;
+  if (num_splits > kMaxSplits ||
+      check_decode(B, H, Hkv, Nq, d, page_size, 1, pages_per_seq, 1.f, FA_BF16, &s) != FA_OK)
+    return 0;
+  return resolve_splits(s.BHkv * s.nqt, s.nkt_max, false, num_splits);
+}
+
+size_t fa_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int d, int page_size,
+                                      int pages_per_seq, int num_splits) {
+  const int S = fa_decode_paged_num_splits(B, H, Hkv, Nq, d, page_size, pages_per_seq, num_splits);
+  if (S < 1) return 0;
+  DecodeShape s;
+  check_decode(B, H, Hkv, Nq, d, page_size, 1, pages_per_seq, 1.f, FA_BF16, &s);
+  return splitkv_ws_bytes(s.BHkv, s.nqt, d, S);
+}
+
+fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_table, const int32_t *seq_len, void *o, float *lse,
+                          int B, int H, int Hkv, int Nq, int d, int page_size, int num_pages,
+                          int pages_per_seq, float scale, fa_dtype dtype, int num_splits,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  DecodeShape s;
+  fa_status r = check_decode(B, H, Hkv, Nq, d, page_size, num_pages, pages_per_seq, scale, dtype, &s);
+  if (r != FA_OK) return r;
+  r = check_ptrs({{q, "q"}, {k_cache, "k_cache"}, {v_cache, "v_cache"}, {o, "o"}, {lse, "lse"}});
+  if (r != FA_OK) return r;
+  for (auto p : {std::make_pair(static_cast<const void *>(block_table), "block_table"),
+                 std::make_pair(static_cast<const void *>(seq_len), "seq_len")}) {
+    if (p.first == nullptr) return fail(FA_ERR_INVALID_ARG, "%s is null", p.second);
+    if (reinterpret_cast<uintptr_t>(p.first) & 3u) return fail(FA_ERR_INVALID_ARG, "%s is not 4-byte aligned", p.second);
+  }
+  if (num_splits > kMaxSplits) return fail(FA_ERR_INVALID_ARG, "num_splits=%d exceeds %d", num_splits, kMaxSplits);
+  const int S = resolve_splits(s.BHkv * s.nqt, s.nkt_max, false, num_splits);
+  if (S > 1) {
+    const size_t need = splitkv_ws_bytes(s.BHkv, s.nqt, d, S);
+    if (workspace == nullptr) return fail(FA_ERR_INVALID_ARG, "workspace is null (num_splits=%d)", S);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(FA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    if (workspace_bytes < need)
+      return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  }
+  CUtensorMap tq, tk, tv;
+  // q [B,H,Nq,d] = [B*Hkv][R][d]: the rows of a key/value head's query heads are contiguous
+  if ((r = make_tile_map(&tq, q, dtype, s.R, s.BHkv, d, "q")) != FA_OK) return r;
+  const long long pool = static_cast<long long>(num_pages) * Hkv;
+  if ((r = make_tile_map(&tk, k_cache, dtype, page_size, pool, d, "k_cache", page_size)) != FA_OK) return r;
+  if ((r = make_tile_map(&tv, v_cache, dtype, page_size, pool, d, "v_cache", page_size)) != FA_OK) return r;
+  fa::FwdArgs a{};
+  a.o = o;
+  a.o_res = nullptr;
+  a.lse = lse;
+  a.kv_len = seq_len;
+  a.block_mask = nullptr;
+  a.H = Hkv;  // the grid runs over (batch, key/value head) blocks of R rows
+  a.N = s.R;
+  a.nqt = s.nqt;
+  a.nkt = s.nkt_max;
+  a.hgroup = 1;
+  a.Hkv = Hkv;
+  a.kv_group = 1;
+  a.num_splits = S;
+  a.o_part = S > 1 ? static_cast<float *>(workspace) : nullptr;
+  a.lse_part = S > 1 ? a.o_part + static_cast<size_t>(S) * s.BHkv * s.nqt * 128 * d : nullptr;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o_scale = 1.f;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.pages_per_seq = pages_per_seq;
+  a.dec_nq = Nq;
+  const int grid = static_cast<int>(s.BHkv * s.nqt);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 64)
+    r = dtype == FA_BF16 ? launch_fwd_t<64, true, false, false, false, true>(tq, tk, tv, a, grid, st)
+                         : launch_fwd_t<64, false, false, false, false, true>(tq, tk, tv, a, grid, st);
+  else
+    r = dtype == FA_BF16 ? launch_fwd_t<128, true, false, false, false, true>(tq, tk, tv, a, grid, st)
+                         : launch_fwd_t<128, false, false, false, false, true>(tq, tk, tv, a, grid, st);
+  if (r != FA_OK) return r;
+  if (S > 1) {
+    const long long rows = s.BHkv * s.R;
+    r = dtype == FA_BF16 ? launch_merge<true>(a, rows, d, st) : launch_merge<false>(a, rows, d, st);
+    if (r != FA_OK) return r;
+  }
   return ok();
 }
 

@@ -56,6 +56,14 @@ struct FwdArgs {
   float *lse_part;
   float scale_log2;
   float o_scale;  // 8-bit forward: V's dequantisation factor, applied to O
+  // paged key/value cache (decode, single-tile kernel): K and V are pools of
+  // pages [num_pages * Hkv][page_size][D] (page-major, then head); key tile
+  // kt of the sequence of batch b gathers the pages block_table[b *
+  // pages_per_seq + kt * 128 / page_size + p]. The query rows of one CTA are
+  // the dec_nq new tokens of each query head of one key/value group; row r
+  // sees keys j <= kv_len[b] - dec_nq + (r % dec_nq).
+  const int32_t *block_table;
+  int page_size, pages_per_seq, dec_nq;
 
   // [B*Hkv] index of the key/value head that query head bh ([B*H] index) reads
   __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
@@ -80,7 +88,9 @@ struct FwdCfg {
   static constexpr int kBPF = kBSF + 2;
   static constexpr int kBOR = kBPF + 2;
   static constexpr int kBDR = kBOR + 1;
-  static constexpr int kNumBars = kBDR + 1;
+  static constexpr int kBVZ = kBDR + 1;  // paged: tail rows of the last V tile zeroed
+  static constexpr int kBVL = kBVZ + 1;  // paged: the last V tile has landed (single use)
+  static constexpr int kNumBars = kBVL + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, list count
   static constexpr int kListOff = kMiscOff + 16;
   static constexpr int kMaxList = 2048;                     // block-sparse: nkt <= 2048
@@ -99,7 +109,7 @@ struct FwdCfg {
 // order. P_lo of tile t is written into the upper half of its own S buffer
 // (already read), and the MMA thread waits for P V of tile t to finish before
 // QK^T of tile t + 2 overwrites that buffer.
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = false>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -121,10 +131,11 @@ __global__ void __launch_bounds__(256, 1)
   if (CAUSAL) qt = a.nqt - 1 - qt;
   const int b = bh / a.H;
   const int kvh = a.kv_head(bh);
-  int kvl = a.N;
+  const int kv_cap = PAGED ? a.pages_per_seq * a.page_size : a.N;
+  int kvl = kv_cap;
   if (a.kv_len != nullptr) {
     const int v = a.kv_len[b];
-    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
+    kvl = v < 0 ? 0 : (v > kv_cap ? kv_cap : v);
   }
   const int nkt_eff = (kvl + 127) >> 7;
 
@@ -142,6 +153,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     mbar_init(bar(C::kBOR), 1);
     mbar_init(bar(C::kBDR), 1);
+    mbar_init(bar(C::kBVZ), 1);
+    mbar_init(bar(C::kBVL), 1);
     *abort_flag = 0u;
     fence_barrier_init();
     prefetch_tensormap(&tm_q);
@@ -174,6 +187,10 @@ __global__ void __launch_bounds__(256, 1)
   const int split = static_cast<int>(blockIdx.y);
   const int t_lo = static_cast<int>(static_cast<long long>(n_all) * split / a.num_splits);
   const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (split + 1) / a.num_splits) - t_lo;
+  // paged: V rows past kv_len in the sequence's last tile hold stale cache
+  // slots (or nothing loaded at all); they are zeroed before P V reads them
+  // so that 0 * (non-finite garbage) cannot reach O
+  const bool zero_tail = PAGED && n_tiles > 0 && t_lo + n_tiles == n_all && (kvl & 127) != 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -189,19 +206,52 @@ __global__ void __launch_bounds__(256, 1)
         const int st = t % C::kStages;
         const uint32_t ph = (t / C::kStages) & 1;
         const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
-        if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
-        for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
-                           bar(C::kBKF + st), kb * 64, kt * 128, kvh, pol_kv);
-        nk = t + 1;
-        if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
-        for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
-                           bar(C::kBVF + st), kb * 64, kt * 128, kvh, pol_kv);
-        nv = t + 1;
+        if constexpr (PAGED) {
+          // the pages of this tile that hold keys < kv_len, gathered page by
+          // page into consecutive rows (page_size x 128 B per column block)
+          const int ppt = 128 / a.page_size;
+          const int npg = min(ppt, (kvl - kt * 128 + a.page_size - 1) / a.page_size);
+          const int32_t *bt = a.block_table + static_cast<size_t>(b) * a.pages_per_seq + kt * ppt;
+          int zc[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p) zc[p] = (p < npg) ? bt[p] * a.Hkv + (bh % a.Hkv) : 0;
+          const uint32_t bytes = static_cast<uint32_t>(npg * a.page_size * D * 2);
+          const uint32_t rowb = static_cast<uint32_t>(a.page_size * 128);
+          if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(C::kBKF + st), bytes);
+          for (int p = 0; p < npg; ++p)
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_k,
+                               bar(C::kBKF + st), kb * 64, 0, zc[p], pol_kv);
+          nk = t + 1;
+          if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(C::kBVF + st), bytes);
+          for (int p = 0; p < npg; ++p)
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_v,
+                               bar(C::kBVF + st), kb * 64, 0, zc[p], pol_kv);
+          nv = t + 1;
+        } else {
+          if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
+          for (int kb = 0; kb < C::kKB; ++kb)
+            tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
+                             bar(C::kBKF + st), kb * 64, kt * 128, kvh, pol_kv);
+          nk = t + 1;
+          if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
+          for (int kb = 0; kb < C::kKB; ++kb)
+            tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
+                             bar(C::kBVF + st), kb * 64, kt * 128, kvh, pol_kv);
+          nv = t + 1;
+        }
       }
+      // paged: the last V tile's full barrier is waited here, by the thread
+      // that loaded it (its phase is unambiguous: the stage's previous phase
+      // completed before this load was issued), then handed to the zeroing warp
+      if (zero_tail && nv == n_tiles &&
+          mbar_wait(bar(C::kBVF + (n_tiles - 1) % C::kStages), ((n_tiles - 1) / C::kStages) & 1, abort_flag))
+        mbar_arrive(bar(C::kBVL));
       if (*abort_flag) {
         // let every copy still in flight land before the CTA exits
         mbar_wait_drain(bar(C::kBQ), 0, abort_flag);
@@ -223,7 +273,11 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t ph = (u / C::kStages) & 1;
         const int pb = u & 1;
         if (!mbar_wait(bar(C::kBPF + pb), (u >> 1) & 1, abort_flag)) return false;
-        if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) return false;
+        if (zero_tail && u == n_tiles - 1) {
+          if (!mbar_wait(bar(C::kBVZ), 0, abort_flag)) return false;
+        } else if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) {
+          return false;
+        }
         tc_fence_after();
         const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
         const uint32_t pcol = tmem + (pb ? C::kColP1 : C::kColP0);
@@ -275,6 +329,24 @@ __global__ void __launch_bounds__(256, 1)
       mma_commit(bar(C::kBDR));
       mbar_wait_drain(bar(C::kBDR), 0, abort_flag);
     }
+  } else if (PAGED && warp == 2) {
+    // ------------------------------------------------------------ V tail
+    if (zero_tail) {
+      const int t = n_tiles - 1;
+      const int st = t % C::kStages;
+      const int valid = kvl - (t_lo + t) * 128;  // 1 .. 127 keys of the tile are real
+      if (mbar_wait_warp(bar(C::kBVL), 0, abort_flag)) {
+        // whole 128-byte rows: the swizzle only permutes 16-byte chunks within a row
+        uint8_t *vt = smem + C::kVOff + st * C::kTileBytes;
+        for (int kb = 0; kb < C::kKB; ++kb)
+          for (int i = lane; i < (128 - valid) * 8; i += 32)
+            *reinterpret_cast<uint4 *>(vt + kb * 16384 + (valid + (i >> 3)) * 128 + (i & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBVZ));
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int row = tid - 128;
@@ -312,6 +384,7 @@ __global__ void __launch_bounds__(256, 1)
       // mask: keys past kv_len / N, and keys after the query on the diagonal
       int limit = kvl - kt * 128;
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
+      if (PAGED) limit = (q_row < a.N) ? limit - a.dec_nq + 1 + q_row % a.dec_nq : 0;
       float m_new, alpha;
       const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
       l = l * alpha + rs;

@@ -14,6 +14,9 @@ Recipe (the pages name BERT-large seq 512, GPT-2 seq 1K, Long-Range-Arena
     generator, drawn after dO;
   * block mask ``torch.rand(nb, nb) < p`` from its own generator
     (``manual_seed(mask_seed)``), diagonal forced to keep;
+  * paged decode: q, then the key and value page pools, drawn as above;
+    context lengths randint(lo, hi + 1); the block table a random
+    permutation of the pool's pages (torch.randperm);
   * 8-bit inputs: q, k, v drawn as above in fp32, each divided by its own
     power-of-two factor 2^ceil(log2(max|x| / 448)) and cast to
     ``torch.float8_e4m3fn`` (round to nearest even; no value reaches the
@@ -47,6 +50,8 @@ class Workload:
     backward: bool = True
     hkv: int | None = None            # key/value heads (grouped-query attention), None = H
     num_splits: int | None = None     # split-KV forward (0 = the library's choice), None = off
+    nq: int | None = None             # paged decode: new tokens per sequence (N = longest context)
+    page_size: int = 0                # paged decode: keys per cache page
     notes: str = field(default="", compare=False)
 
     @property
@@ -83,6 +88,11 @@ WORKLOADS = {
     # the N = 8192 long-context point with 8-bit q, k, v
     "fp8_b4_h16_n8192_d128_e4m3_causal": Workload(
         "fp8_b4_h16_n8192_d128_e4m3_causal", 4, 16, 8192, 128, "e4m3", causal=True, backward=False),
+    # serving-shaped decode: 32 sequences of 4K-8K cached tokens in 16-token
+    # pages, 32 query heads on 8 key/value heads, one new token each
+    "decode_b32_h32_hkv8_nq1_ctx4k8k_d128_bf16_page16": Workload(
+        "decode_b32_h32_hkv8_nq1_ctx4k8k_d128_bf16_page16", 32, 32, 8192, 128, "bf16",
+        kv_len_range=(4096, 8192), hkv=8, nq=1, page_size=16, backward=False, num_splits=0),
     # one long head: 64 query tiles cannot fill 148 SMs without splitting the keys
     "splitkv_b1_h1_n8192_d128_bf16": Workload(
         "splitkv_b1_h1_n8192_d128_bf16", 1, 1, 8192, 128, "bf16", qk_mult=2.0, backward=False,
@@ -145,6 +155,28 @@ def make_qkv_fp8(B, H, N, d, seed=0, hkv=None, kv_len_range=None):
     return out
 
 
+def make_paged_decode(B, H, Hkv, Nq, d, dtype, page_size, ctx_range, seed=0, spare_pages=0):
+    """Decode inputs over a paged cache: q [B,H,Nq,d]; k_cache, v_cache
+    [num_pages, Hkv, page_size, d] drawn N(0,1) and cast like make_qkv;
+    seq_len int32 [B] = randint(lo, hi + 1); block_table int32 [B,
+    pages_per_seq] (pages_per_seq = ceil(hi / page_size)) holding a random
+    permutation of the pool, whose size is B * pages_per_seq + spare_pages
+    (pages no sequence uses)."""
+    tdt = torch.float16 if dtype in ("f16", torch.float16) else torch.bfloat16
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    lo, hi = ctx_range
+    pages_per_seq = -(-hi // page_size)
+    num_pages = B * pages_per_seq + spare_pages
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(tdt)
+    k = torch.randn((num_pages, Hkv, page_size, d), generator=g, dtype=torch.float32).to(tdt)
+    v = torch.randn((num_pages, Hkv, page_size, d), generator=g, dtype=torch.float32).to(tdt)
+    seq_len = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    perm = torch.randperm(num_pages, generator=g)[: B * pages_per_seq]
+    block_table = perm.reshape(B, pages_per_seq).to(torch.int32)
+    return {"q": q, "k_cache": k, "v_cache": v, "seq_len": seq_len, "block_table": block_table,
+            "page_size": page_size}
+
+
 def dequant(x8, descale):
     """Real values of an e4m3 tensor (exact in fp64)."""
     return x8.to(torch.float64) * descale
@@ -154,6 +186,9 @@ def make_workload(w: Workload, with_dout=None):
     """All inputs of a named workload (CPU tensors)."""
     if with_dout is None:
         with_dout = w.backward
+    if w.nq is not None:
+        return make_paged_decode(w.B, w.H, w.hkv or w.H, w.nq, w.d, w.dtype, w.page_size, w.kv_len_range,
+                                 seed=w.seed)
     if w.dtype == "e4m3":
         return make_qkv_fp8(w.B, w.H, w.N, w.d, seed=w.seed, hkv=w.hkv, kv_len_range=w.kv_len_range)
     t = make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult,

@@ -189,6 +189,54 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float
 size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
 
 /*
+ * Decode attention over a paged key/value cache ("Enhancing Transformer
+ * Models: Innovations in Attention Mechanisms and Performance Optimization",
+ * section "From FlashAttention to PagedAttention", which presents
+ * PagedAttention as page-wise management of the data moved between HBM and
+ * on-chip memory; the arithmetic per query row is exact attention as in
+ * fa_fwd_gqa).
+ *   q       [B,H,Nq,d] 16-bit: the Nq newest tokens of each of B sequences.
+ *   k_cache, v_cache  [num_pages, Hkv, page_size, d] 16-bit page pools: page
+ *           p holds page_size consecutive key (value) rows of every
+ *           key/value head.
+ *   block_table  DEVICE int32 [B, pages_per_seq]: logical page i of
+ *           sequence b is pool page block_table[b * pages_per_seq + i].
+ *           Entries must lie in [0, num_pages) for the pages that hold keys
+ *           below seq_len[b]; entries past them are not read. An entry
+ *           outside the pool reads as zero keys and values.
+ *   seq_len DEVICE int32 [B]: keys of sequence b (the cached context,
+ *           including the Nq new tokens); values above pages_per_seq *
+ *           page_size act as that, values below 1 mask every key. Cache
+ *           slots past seq_len may hold anything (they are never used).
+ *   o [B,H,Nq,d] out (same 16-bit type); lse [B,H,Nq] fp32 out.
+ *   Query i (0-based among the Nq) of sequence b sees keys
+ *   j <= seq_len[b] - Nq + i (the new tokens attend causally to each other
+ *   and to the whole cached prefix); query head h reads key/value head
+ *   h / (H / Hkv). A query with no visible key gets O = 0, LSE = -inf.
+ *   page_size in {16, 32, 64, 128}; d in {64, 128}; H % Hkv == 0.
+ *   num_splits, workspace: as for fa_fwd_splitkv (the key tiles of each
+ *   sequence are shared by S CTAs and merged); the workspace size is
+ *   fa_decode_paged_workspace_size.
+ */
+fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_table, const int32_t *seq_len, void *o, float *lse,
+                          int B, int H, int Hkv, int Nq, int d, int page_size, int num_pages,
+                          int pages_per_seq, float scale, fa_dtype dtype, int num_splits,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* The S fa_decode_paged uses (num_splits >= 1: itself; <= 0: the library's
+ * choice for sequences of up to pages_per_seq * page_size keys); 0 for
+ * invalid sizes. */
+int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_size,
+                               int pages_per_seq, int num_splits);
+
+/* Workspace bytes of fa_decode_paged: with R = ceil(H / Hkv * Nq / 128) *
+ * 128 rows per (b, key/value head), S * B * Hkv * R * (d + 1) * 4; 0 when
+ * S == 1 or for invalid sizes. */
+size_t fa_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int d, int page_size,
+                                      int pages_per_seq, int num_splits);
+
+/*
  * The S fa_fwd_splitkv uses for these arguments (num_splits >= 1: itself;
  * <= 0: the library's choice for the current device), 0 for invalid sizes.
  */

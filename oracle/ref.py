@@ -219,7 +219,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_len, scale, page_size, li
     block_table [B, pages_per_seq]; seq_len [B]. Returns o [B,H,Nq,d] and
     lse [B,H,Nq] (float64; a query with no visible key: 0 and -inf).
     """
-    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    q = _f64(q)
+    kc, vc = k_cache, v_cache  # widened page by page below (the pool may be large)
     bt = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table)
     sl = np.asarray(seq_len.cpu().numpy() if hasattr(seq_len, "cpu") else seq_len)
     B, H, Nq, d = q.shape
@@ -233,8 +234,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_len, scale, page_size, li
             continue
         pages = bt[b, :(L + page_size - 1) // page_size]
         for kvh in range(Hkv):
-            keys = np.concatenate([kc[p, kvh] for p in pages], axis=0)[:L]
-            vals = np.concatenate([vc[p, kvh] for p in pages], axis=0)[:L]
+            keys = np.concatenate([_f64(kc[p, kvh]) for p in pages], axis=0)[:L]
+            vals = np.concatenate([_f64(vc[p, kvh]) for p in pages], axis=0)[:L]
             for h in range(kvh * (H // Hkv), (kvh + 1) * (H // Hkv)):
                 pos = [L - Nq + i for i in range(Nq)]
                 live = [i for i in range(Nq) if pos[i] >= 0]

@@ -145,6 +145,26 @@ def test_fp8_sizes_and_argument_checks():
     assert call(q=FAKE + 8) == 1                 # q not 16-byte aligned
 
 
+def test_decode_sizes_and_argument_checks():
+    lib = fa.load_library()
+    # R = 4 query rows per (b, kv head) -> one 128-row tile; 3 shares
+    assert fa.fa_decode_paged_workspace_size(2, 8, 2, 1, 128, 16, 64, 3) == 3 * 2 * 2 * 128 * 129 * 4
+    assert fa.fa_decode_paged_workspace_size(2, 8, 2, 1, 128, 16, 64, 1) == 0
+    assert fa.fa_decode_paged_num_splits(2, 8, 2, 1, 128, 16, 64, 5) == 5
+    assert fa.fa_decode_paged_num_splits(2, 8, 2, 1, 128, 24, 64, 5) == 0   # page size not built
+    assert 2 <= fa.fa_decode_paged_num_splits(1, 8, 8, 1, 128, 16, 512, 0) <= 64
+    f = ctypes.c_float
+
+    def call(H=8, Hkv=2, Nq=1, d=128, ps=16, num_pages=64, pps=8, bt=FAKE, sl=FAKE, S=1, ws=None, wsb=0):
+        return lib.fa_decode_paged(FAKE, FAKE, FAKE, bt, sl, FAKE, FAKE, 2, H, Hkv, Nq, d, ps, num_pages, pps,
+                                   f(0.1), 1, S, ws, wsb, None)
+    assert call(ps=8) == 2 and call(ps=256) == 2 and call(d=96) == 2
+    assert call(Hkv=3) == 1 and call(Nq=0) == 1 and call(num_pages=0) == 1 and call(pps=0) == 1
+    assert call(bt=None) == 1 and call(sl=FAKE + 2) == 1
+    assert call(S=4) == 1                        # shares need a workspace
+    assert call(S=4, ws=FAKE + 16, wsb=1 << 30) == 1
+
+
 def test_blocksparse_rejects_missing_mask():
     lib = fa.load_library()
     st = lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, ctypes.c_float(0.1), 0,
