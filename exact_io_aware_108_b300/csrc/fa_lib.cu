@@ -164,7 +164,7 @@ template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = f
 fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
   auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT, PAGED>;
-  constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
+  constexpr int smem = fa::FwdCfg<D, PAGED>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
   kern<<<dim3(grid, a.num_splits), 256, smem, st>>>(tq, tk, tv, a);
@@ -296,6 +296,20 @@ int resolve_splits(long long ctas, int nkt, bool causal, int requested) {
     }
   }
   return best;
+}
+
+// Decode split factor: the request when it is >= 1, else the smallest S
+// that gives about 7 waves of CTAs, with at least 16 key tiles of the
+// longest sequence per share, at most 64 shares. The key walk is bound by
+// HBM: many CTAs let the block scheduler balance sequences of unequal
+// length, while short shares pay their start-up (first K/V latency) and
+// partial-result traffic too often (measured on 32 and 4 sequences of
+// 4K-8K and 16K-32K keys, page sizes 16 and 128).
+int resolve_decode_splits(long long ctas, int nkt_max, int requested) {
+  if (requested >= 1) return requested;
+  const long long want = (7 * static_cast<long long>(sm_count()) + ctas - 1) / ctas;
+  const long long cap = std::max(1, std::min(64, nkt_max / 16));
+  return static_cast<int>(std::max(1ll, std::min(want, cap)));
 }
 
 // Split-KV workspace: fp32 O / l [S][R][d] then fp32 LSE [S][R], R = B*H*nqt*128.
@@ -640,7 +654,7 @@ fa_status check_decode(int B, int H, int Hkv, int Nq, int d, int page_size, int 
   if (R > (1 << 20)) return fail(FA_ERR_INVALID_ARG, "(H / Hkv) * Nq too large");
   s->BHkv = static_cast<long long>(B) * Hkv;
   s->R = static_cast<int>(R);
-  s->nqt = static_cast<int>((R + 127) / 128);
+  s->nqt = static_cast<int>((R + fa::FwdCfg<64, true>::kQRows - 1) / fa::FwdCfg<64, true>::kQRows);
   s->nkt_max = static_cast<int>((static_cast<long long>(pages_per_seq) * page_size + 127) / 128);
   if (s->BHkv * s->nqt > INT_MAX) return fail(FA_ERR_INVALID_ARG, "grid too large");
   return FA_OK;
@@ -718,7 +732,7 @@ int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_si
   if (num_splits > kMaxSplits ||
       check_decode(B, H, Hkv, Nq, d, page_size, 1, pages_per_seq, 1.f, FA_BF16, &s) != FA_OK)
     return 0;
-  return resolve_splits(s.BHkv * s.nqt, s.nkt_max, false, num_splits);
+  return resolve_decode_splits(s.BHkv * s.nqt, s.nkt_max, num_splits);
 }
 
 size_t fa_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int d, int page_size,
@@ -746,7 +760,7 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
     if (reinterpret_cast<uintptr_t>(p.first) & 3u) return fail(FA_ERR_INVALID_ARG, "%s is not 4-byte aligned", p.second);
   }
   if (num_splits > kMaxSplits) return fail(FA_ERR_INVALID_ARG, "num_splits=%d exceeds %d", num_splits, kMaxSplits);
-  const int S = resolve_splits(s.BHkv * s.nqt, s.nkt_max, false, num_splits);
+  const int S = resolve_decode_splits(s.BHkv * s.nqt, s.nkt_max, num_splits);
   if (S > 1) {
     const size_t need = splitkv_ws_bytes(s.BHkv, s.nqt, d, S);
     if (workspace == nullptr) return fail(FA_ERR_INVALID_ARG, "workspace is null (num_splits=%d)", S);
@@ -757,7 +771,7 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
   }
   CUtensorMap tq, tk, tv;
   // q [B,H,Nq,d] = [B*Hkv][R][d]: the rows of a key/value head's query heads are contiguous
-  if ((r = make_tile_map(&tq, q, dtype, s.R, s.BHkv, d, "q")) != FA_OK) return r;
+  if ((r = make_tile_map(&tq, q, dtype, s.R, s.BHkv, d, "q", fa::FwdCfg<64, true>::kQRows)) != FA_OK) return r;
   const long long pool = static_cast<long long>(num_pages) * Hkv;
   if ((r = make_tile_map(&tk, k_cache, dtype, page_size, pool, d, "k_cache", page_size)) != FA_OK) return r;
   if ((r = make_tile_map(&tv, v_cache, dtype, page_size, pool, d, "v_cache", page_size)) != FA_OK) return r;

@@ -61,7 +61,9 @@ struct FwdArgs {
   // kt of the sequence of batch b gathers the pages block_table[b *
   // pages_per_seq + kt * 128 / page_size + p]. The query rows of one CTA are
   // the dec_nq new tokens of each query head of one key/value group; row r
-  // sees keys j <= kv_len[b] - dec_nq + (r % dec_nq).
+  // sees keys j <= kv_len[b] - dec_nq + (r % dec_nq). A paged K or V tile
+  // has the dense layout: page p of the tile fills rows [p * page_size,
+  // (p + 1) * page_size) of each 128-byte column block, one TMA box each.
   const int32_t *block_table;
   int page_size, pages_per_seq, dec_nq;
 
@@ -69,13 +71,20 @@ struct FwdArgs {
   __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
 };
 
-template <int D>
+template <int D, bool PAGED = false>
 struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile, 16-bit
-  static constexpr int kStages = (D == 64) ? 4 : 2; // K/V ring depth
+  // paged decode: query blocks of 64 rows (a key/value head's query heads
+  // times the new tokens; more rows take more query tiles), which frees the
+  // shared memory of a third K/V stage at d = 128. The M = 128 products then
+  // read rows 64..127 of "Q" from the memory after it: they feed only
+  // padding rows of S, P and O, which are never used.
+  static constexpr int kQRows = PAGED ? 64 : 128;
+  static constexpr int kQColBlock = kQRows * 128;   // bytes of one 128-byte-wide Q column block
+  static constexpr int kStages = PAGED ? (D == 64 ? 6 : 3) : (D == 64 ? 4 : 2);  // K/V ring depth
   static constexpr int kKB = D / 64;                // 128-byte column blocks
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kTileBytes;
+  static constexpr int kKOff = kQColBlock * kKB;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O ready, drain
@@ -113,7 +122,7 @@ template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = f
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, PAGED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = align_up_1024(raw);
@@ -196,12 +205,25 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_tiles > 0) {
       const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes);
+      // K/V are re-read by the other query tiles of a head (keep them in L2)
+      // except in decode, where each cache page is read exactly once
+      const uint64_t pol_kv = PAGED ? policy_evict_first() : policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBQ), C::kQColBlock * C::kKB);
       for (int kb = 0; kb < C::kKB; ++kb)
-        tma_load_3d_hint(sbase + C::kQOff + kb * 16384, &tm_q, bar(C::kBQ), kb * 64, qt * 128, bh,
+        tma_load_3d_hint(sbase + C::kQOff + kb * C::kQColBlock, &tm_q, bar(C::kBQ), kb * 64, qt * C::kQRows, bh,
                          pol_q);
       int nk = 0, nv = 0;
+      // paged: pool coordinates of the pages of the next tile, read one tile
+      // ahead so that the block-table latency overlaps the current tile's waits
+      const int ppt = PAGED ? 128 / a.page_size : 0;
+      const int32_t *bt_row = PAGED ? a.block_table + static_cast<size_t>(b) * a.pages_per_seq : nullptr;
+      auto pages_of = [&](int kt) { return min(ppt, (kvl - kt * 128 + a.page_size - 1) / a.page_size); };
+      int zc_next[8];
+      if constexpr (PAGED) {
+        const int np0 = pages_of(t_lo);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) zc_next[p] = (p < np0) ? bt_row[t_lo * ppt + p] * a.Hkv + (bh % a.Hkv) : 0;
+      }
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % C::kStages;
         const uint32_t ph = (t / C::kStages) & 1;
@@ -209,27 +231,35 @@ __global__ void __launch_bounds__(256, 1)
         if constexpr (PAGED) {
           // the pages of this tile that hold keys < kv_len, gathered page by
           // page into consecutive rows (page_size x 128 B per column block)
-          const int ppt = 128 / a.page_size;
-          const int npg = min(ppt, (kvl - kt * 128 + a.page_size - 1) / a.page_size);
-          const int32_t *bt = a.block_table + static_cast<size_t>(b) * a.pages_per_seq + kt * ppt;
+          const int npg = pages_of(kt);
           int zc[8];
 #pragma unroll
-          for (int p = 0; p < 8; ++p) zc[p] = (p < npg) ? bt[p] * a.Hkv + (bh % a.Hkv) : 0;
+          for (int p = 0; p < 8; ++p) zc[p] = zc_next[p];
+          if (t + 1 < n_tiles) {
+            const int np1 = pages_of(kt + 1);
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              zc_next[p] = (p < np1) ? bt_row[(kt + 1) * ppt + p] * a.Hkv + (bh % a.Hkv) : 0;
+          }
           const uint32_t bytes = static_cast<uint32_t>(npg * a.page_size * D * 2);
           const uint32_t rowb = static_cast<uint32_t>(a.page_size * 128);
           if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
           mbar_arrive_expect_tx(bar(C::kBKF + st), bytes);
-          for (int p = 0; p < npg; ++p)
-            for (int kb = 0; kb < C::kKB; ++kb)
-              tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_k,
-                               bar(C::kBKF + st), kb * 64, 0, zc[p], pol_kv);
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+            if (p < npg)
+              for (int kb = 0; kb < C::kKB; ++kb)
+                tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_k,
+                                 bar(C::kBKF + st), kb * 64, 0, zc[p], pol_kv);
           nk = t + 1;
           if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
           mbar_arrive_expect_tx(bar(C::kBVF + st), bytes);
-          for (int p = 0; p < npg; ++p)
-            for (int kb = 0; kb < C::kKB; ++kb)
-              tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_v,
-                               bar(C::kBVF + st), kb * 64, 0, zc[p], pol_kv);
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+            if (p < npg)
+              for (int kb = 0; kb < C::kKB; ++kb)
+                tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_v,
+                                 bar(C::kBVF + st), kb * 64, 0, zc[p], pol_kv);
           nv = t + 1;
         } else {
           if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
@@ -281,22 +311,24 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
         const uint32_t pcol = tmem + (pb ? C::kColP1 : C::kColP0);
-        // two halves of 64 keys, high then low part of each (the product
-        // order of the two-tile kernel, so both round O identically)
+        {
+          // two halves of 64 keys, high then low part of each (the product
+          // order of the two-tile kernel, so both round O identically)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int ks = 4 * h; ks < 4 * h + 4; ++ks) {
-            // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
-            const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
-            mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
-          }
-          if constexpr (SPLIT) {
-            const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
+            for (int ks = 4 * h; ks < 4 * h + 4; ++ks) {
+              // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
+              const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
+              mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
+            }
+            if constexpr (SPLIT) {
+              const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
 #pragma unroll
-            for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-              mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
-                     kIdPV, 1u);
+              for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
+                mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
+                       kIdPV, 1u);
+            }
           }
         }
         mma_commit(bar(C::kBVE + st));
@@ -316,9 +348,11 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           // A = Q, B = K_j, both K-major: 16 head-dim elements = 32 B per step
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          // (Q's column blocks are kQColBlock bytes apart, K's 16 KB)
+          const uint32_t qoff = (ks >> 2) * C::kQColBlock + (ks & 3) * 32;
+          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + qoff, 16, 1024),
+                 sdesc_sw128(kbase + koff, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF + sb));
         mma_commit(bar(C::kBKE + st));
@@ -351,14 +385,24 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ softmax
     const int row = tid - 128;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int q_row = qt * 128 + row;
+    const int q_row = qt * C::kQRows + row;
     const float sl2 = a.scale_log2;
+    // every row of this warp lies past N (the last query tile; the padding of
+    // a decode block): its P rows feed only O rows that are never stored, so
+    // it skips the softmax and only keeps the P barrier's count in step.
+    // S(t) complete implies the P barrier's previous phase of this buffer
+    // completed (S(t) overwrote S(t-2) after P(t-2) arrived).
+    const bool pad_warp = (warp & 3) * 32 >= C::kQRows || qt * C::kQRows + (warp & 3) * 32 >= a.N;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const int sb = t & 1;
       const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
       if (!mbar_wait_warp(bar(C::kBSF + sb), (t >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (pad_warp) {
+        mbar_arrive(bar(C::kBPF + sb));
+        continue;
+      }
       tc_fence_after();
       float s[128];
       {
@@ -423,6 +467,7 @@ __global__ void __launch_bounds__(256, 1)
       m = m_new;
     }
     // ---- epilogue: O / l and LSE
+    if (!pad_warp) {
     bool have_o = ok && n_tiles > 0;
     if (have_o) {
       have_o = mbar_wait_warp(bar(C::kBOR), (n_tiles - 1) & 1, abort_flag);
@@ -445,9 +490,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) oall[j][i] = 0u;
     }
-    if (a.num_splits > 1) {
-      // split-KV partial: O / l in fp32 and this share's LSE (rows past N
-      // included: the merge reads only rows < N)
+    if (a.num_splits > 1 && q_row < a.N) {
+      // split-KV partial: O / l in fp32 and this share's LSE (the merge
+      // reads only rows < N)
       const size_t prow = static_cast<size_t>(split) * a.nqt * 128 * (gridDim.x / a.nqt) +
                           static_cast<size_t>(bh) * a.nqt * 128 + static_cast<size_t>(q_row);
       float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * D);
@@ -458,7 +503,7 @@ __global__ void __launch_bounds__(256, 1)
           dst[(32 * j + i) / 4] = make_float4(__uint_as_float(oall[j][i]) * inv_l, __uint_as_float(oall[j][i + 1]) * inv_l,
                                               __uint_as_float(oall[j][i + 2]) * inv_l, __uint_as_float(oall[j][i + 3]) * inv_l);
       a.lse_part[prow] = lse_row;
-    } else {
+    } else if (a.num_splits == 1) {
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       const uint32_t (&o)[32] = oall[c0 / 32];
@@ -484,6 +529,7 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     if (q_row < a.N) a.lse[static_cast<size_t>(bh) * a.N + q_row] = lse_row;
+    }
     }
   }
 

@@ -215,7 +215,9 @@ size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
  *   h / (H / Hkv). A query with no visible key gets O = 0, LSE = -inf.
  *   page_size in {16, 32, 64, 128}; d in {64, 128}; H % Hkv == 0.
  *   num_splits, workspace: as for fa_fwd_splitkv (the key tiles of each
- *   sequence are shared by S CTAs and merged); the workspace size is
+ *   sequence are shared by S CTAs and merged); num_splits <= 0 picks the
+ *   smallest S giving about 7 waves of CTAs, with at least 16 key tiles
+ *   of the longest sequence per share. The workspace size is
  *   fa_decode_paged_workspace_size.
  */
 fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
@@ -230,9 +232,9 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
 int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_size,
                                int pages_per_seq, int num_splits);
 
-/* Workspace bytes of fa_decode_paged: with R = ceil(H / Hkv * Nq / 128) *
- * 128 rows per (b, key/value head), S * B * Hkv * R * (d + 1) * 4; 0 when
- * S == 1 or for invalid sizes. */
+/* Workspace bytes of fa_decode_paged: with T = ceil(H / Hkv * Nq / 64)
+ * query tiles per (b, key/value head), S * B * Hkv * T * 128 * (d + 1) * 4;
+ * 0 when S == 1 or for invalid sizes. */
 size_t fa_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int d, int page_size,
                                       int pages_per_seq, int num_splits);
 
