@@ -18,6 +18,7 @@
 #include "fwd_kernel.cuh"
 #include "fwd2_kernel.cuh"
 #include "fwd_fp8.cuh"
+#include "decode_kernel.cuh"
 #include "bwd_kernel.cuh"
 
 namespace {
@@ -160,11 +161,11 @@ cudaError_t set_smem(const void *kernel, int bytes) {
   return e;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = false>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
 fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
-  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT, PAGED>;
-  constexpr int smem = fa::FwdCfg<D, PAGED>::kSmemBytes;
+  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT>;
+  constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
   kern<<<dim3(grid, a.num_splits), 256, smem, st>>>(tq, tk, tv, a);
@@ -207,6 +208,20 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   e = cudaGetLastError();
   *r = (e != cudaSuccess) ? cuda_fail(e, "fwd2 launch") : FA_OK;
   return true;
+}
+
+// Paged decode: two CTAs per SM (128 threads, DecCfg<D>::kSmemBytes each).
+template <int D, bool BF16>
+fa_status launch_decode(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
+  auto kern = fa::decode_kernel<D, BF16>;
+  constexpr int smem = fa::DecCfg<D>::kSmemBytes;
+  cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
+  kern<<<dim3(grid, a.num_splits), 128, smem, st>>>(tq, tk, tv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return FA_OK;
 }
 
 // Split-KV merge: one thread per 4 channels of a query row.
@@ -654,7 +669,7 @@ fa_status check_decode(int B, int H, int Hkv, int Nq, int d, int page_size, int 
   if (R > (1 << 20)) return fail(FA_ERR_INVALID_ARG, "(H / Hkv) * Nq too large");
   s->BHkv = static_cast<long long>(B) * Hkv;
   s->R = static_cast<int>(R);
-  s->nqt = static_cast<int>((R + fa::FwdCfg<64, true>::kQRows - 1) / fa::FwdCfg<64, true>::kQRows);
+  s->nqt = static_cast<int>((R + fa::DecCfg<64>::kQRows - 1) / fa::DecCfg<64>::kQRows);
   s->nkt_max = static_cast<int>((static_cast<long long>(pages_per_seq) * page_size + 127) / 128);
   if (s->BHkv * s->nqt > INT_MAX) return fail(FA_ERR_INVALID_ARG, "grid too large");
   return FA_OK;
@@ -771,7 +786,7 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
   }
   CUtensorMap tq, tk, tv;
   // q [B,H,Nq,d] = [B*Hkv][R][d]: the rows of a key/value head's query heads are contiguous
-  if ((r = make_tile_map(&tq, q, dtype, s.R, s.BHkv, d, "q", fa::FwdCfg<64, true>::kQRows)) != FA_OK) return r;
+  if ((r = make_tile_map(&tq, q, dtype, s.R, s.BHkv, d, "q", fa::DecCfg<64>::kQRows)) != FA_OK) return r;
   const long long pool = static_cast<long long>(num_pages) * Hkv;
   if ((r = make_tile_map(&tk, k_cache, dtype, page_size, pool, d, "k_cache", page_size)) != FA_OK) return r;
   if ((r = make_tile_map(&tv, v_cache, dtype, page_size, pool, d, "v_cache", page_size)) != FA_OK) return r;
@@ -800,11 +815,11 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
   const int grid = static_cast<int>(s.BHkv * s.nqt);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    r = dtype == FA_BF16 ? launch_fwd_t<64, true, false, false, false, true>(tq, tk, tv, a, grid, st)
-                         : launch_fwd_t<64, false, false, false, false, true>(tq, tk, tv, a, grid, st);
+    r = dtype == FA_BF16 ? launch_decode<64, true>(tq, tk, tv, a, grid, st)
+                         : launch_decode<64, false>(tq, tk, tv, a, grid, st);
   else
-    r = dtype == FA_BF16 ? launch_fwd_t<128, true, false, false, false, true>(tq, tk, tv, a, grid, st)
-                         : launch_fwd_t<128, false, false, false, false, true>(tq, tk, tv, a, grid, st);
+    r = dtype == FA_BF16 ? launch_decode<128, true>(tq, tk, tv, a, grid, st)
+                         : launch_decode<128, false>(tq, tk, tv, a, grid, st);
   if (r != FA_OK) return r;
   if (S > 1) {
     const long long rows = s.BHkv * s.R;

@@ -56,14 +56,10 @@ struct FwdArgs {
   float *lse_part;
   float scale_log2;
   float o_scale;  // 8-bit forward: V's dequantisation factor, applied to O
-  // paged key/value cache (decode, single-tile kernel): K and V are pools of
-  // pages [num_pages * Hkv][page_size][D] (page-major, then head); key tile
-  // kt of the sequence of batch b gathers the pages block_table[b *
-  // pages_per_seq + kt * 128 / page_size + p]. The query rows of one CTA are
-  // the dec_nq new tokens of each query head of one key/value group; row r
-  // sees keys j <= kv_len[b] - dec_nq + (r % dec_nq). A paged K or V tile
-  // has the dense layout: page p of the tile fills rows [p * page_size,
-  // (p + 1) * page_size) of each 128-byte column block, one TMA box each.
+  // paged key/value cache (decode_kernel.cuh): K and V are pools of pages
+  // [num_pages * Hkv][page_size][D]; page p of key tile kt of the sequence
+  // of batch b is block_table[b * pages_per_seq + kt * 128 / page_size + p];
+  // dec_nq new tokens per sequence and query head.
   const int32_t *block_table;
   int page_size, pages_per_seq, dec_nq;
 
@@ -71,20 +67,13 @@ struct FwdArgs {
   __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
 };
 
-template <int D, bool PAGED = false>
+template <int D>
 struct FwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile, 16-bit
-  // paged decode: query blocks of 64 rows (a key/value head's query heads
-  // times the new tokens; more rows take more query tiles), which frees the
-  // shared memory of a third K/V stage at d = 128. The M = 128 products then
-  // read rows 64..127 of "Q" from the memory after it: they feed only
-  // padding rows of S, P and O, which are never used.
-  static constexpr int kQRows = PAGED ? 64 : 128;
-  static constexpr int kQColBlock = kQRows * 128;   // bytes of one 128-byte-wide Q column block
-  static constexpr int kStages = PAGED ? (D == 64 ? 6 : 3) : (D == 64 ? 4 : 2);  // K/V ring depth
+  static constexpr int kStages = (D == 64) ? 4 : 2; // K/V ring depth
   static constexpr int kKB = D / 64;                // 128-byte column blocks
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQColBlock * kKB;
+  static constexpr int kKOff = kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O ready, drain
@@ -97,9 +86,7 @@ struct FwdCfg {
   static constexpr int kBPF = kBSF + 2;
   static constexpr int kBOR = kBPF + 2;
   static constexpr int kBDR = kBOR + 1;
-  static constexpr int kBVZ = kBDR + 1;  // paged: tail rows of the last V tile zeroed
-  static constexpr int kBVL = kBVZ + 1;  // paged: the last V tile has landed (single use)
-  static constexpr int kNumBars = kBVL + 1;
+  static constexpr int kNumBars = kBDR + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, list count
   static constexpr int kListOff = kMiscOff + 16;
   static constexpr int kMaxList = 2048;                     // block-sparse: nkt <= 2048
@@ -118,11 +105,11 @@ struct FwdCfg {
 // order. P_lo of tile t is written into the upper half of its own S buffer
 // (already read), and the MMA thread waits for P V of tile t to finish before
 // QK^T of tile t + 2 overwrites that buffer.
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT, bool PAGED = false>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using C = FwdCfg<D, PAGED>;
+  using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = align_up_1024(raw);
@@ -140,11 +127,10 @@ __global__ void __launch_bounds__(256, 1)
   if (CAUSAL) qt = a.nqt - 1 - qt;
   const int b = bh / a.H;
   const int kvh = a.kv_head(bh);
-  const int kv_cap = PAGED ? a.pages_per_seq * a.page_size : a.N;
-  int kvl = kv_cap;
+  int kvl = a.N;
   if (a.kv_len != nullptr) {
     const int v = a.kv_len[b];
-    kvl = v < 0 ? 0 : (v > kv_cap ? kv_cap : v);
+    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
   }
   const int nkt_eff = (kvl + 127) >> 7;
 
@@ -162,8 +148,6 @@ __global__ void __launch_bounds__(256, 1)
     }
     mbar_init(bar(C::kBOR), 1);
     mbar_init(bar(C::kBDR), 1);
-    mbar_init(bar(C::kBVZ), 1);
-    mbar_init(bar(C::kBVL), 1);
     *abort_flag = 0u;
     fence_barrier_init();
     prefetch_tensormap(&tm_q);
@@ -196,92 +180,34 @@ __global__ void __launch_bounds__(256, 1)
   const int split = static_cast<int>(blockIdx.y);
   const int t_lo = static_cast<int>(static_cast<long long>(n_all) * split / a.num_splits);
   const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (split + 1) / a.num_splits) - t_lo;
-  // paged: V rows past kv_len in the sequence's last tile hold stale cache
-  // slots (or nothing loaded at all); they are zeroed before P V reads them
-  // so that 0 * (non-finite garbage) cannot reach O
-  const bool zero_tail = PAGED && n_tiles > 0 && t_lo + n_tiles == n_all && (kvl & 127) != 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_tiles > 0) {
       const uint64_t pol_q = policy_evict_first();
-      // K/V are re-read by the other query tiles of a head (keep them in L2)
-      // except in decode, where each cache page is read exactly once
-      const uint64_t pol_kv = PAGED ? policy_evict_first() : policy_evict_last();
-      mbar_arrive_expect_tx(bar(C::kBQ), C::kQColBlock * C::kKB);
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes);
       for (int kb = 0; kb < C::kKB; ++kb)
-        tma_load_3d_hint(sbase + C::kQOff + kb * C::kQColBlock, &tm_q, bar(C::kBQ), kb * 64, qt * C::kQRows, bh,
+        tma_load_3d_hint(sbase + C::kQOff + kb * 16384, &tm_q, bar(C::kBQ), kb * 64, qt * 128, bh,
                          pol_q);
       int nk = 0, nv = 0;
-      // paged: pool coordinates of the pages of the next tile, read one tile
-      // ahead so that the block-table latency overlaps the current tile's waits
-      const int ppt = PAGED ? 128 / a.page_size : 0;
-      const int32_t *bt_row = PAGED ? a.block_table + static_cast<size_t>(b) * a.pages_per_seq : nullptr;
-      auto pages_of = [&](int kt) { return min(ppt, (kvl - kt * 128 + a.page_size - 1) / a.page_size); };
-      int zc_next[8];
-      if constexpr (PAGED) {
-        const int np0 = pages_of(t_lo);
-#pragma unroll
-        for (int p = 0; p < 8; ++p) zc_next[p] = (p < np0) ? bt_row[t_lo * ppt + p] * a.Hkv + (bh % a.Hkv) : 0;
-      }
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % C::kStages;
         const uint32_t ph = (t / C::kStages) & 1;
         const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
-        if constexpr (PAGED) {
-          // the pages of this tile that hold keys < kv_len, gathered page by
-          // page into consecutive rows (page_size x 128 B per column block)
-          const int npg = pages_of(kt);
-          int zc[8];
-#pragma unroll
-          for (int p = 0; p < 8; ++p) zc[p] = zc_next[p];
-          if (t + 1 < n_tiles) {
-            const int np1 = pages_of(kt + 1);
-#pragma unroll
-            for (int p = 0; p < 8; ++p)
-              zc_next[p] = (p < np1) ? bt_row[(kt + 1) * ppt + p] * a.Hkv + (bh % a.Hkv) : 0;
-          }
-          const uint32_t bytes = static_cast<uint32_t>(npg * a.page_size * D * 2);
-          const uint32_t rowb = static_cast<uint32_t>(a.page_size * 128);
-          if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(C::kBKF + st), bytes);
-#pragma unroll
-          for (int p = 0; p < 8; ++p)
-            if (p < npg)
-              for (int kb = 0; kb < C::kKB; ++kb)
-                tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_k,
-                                 bar(C::kBKF + st), kb * 64, 0, zc[p], pol_kv);
-          nk = t + 1;
-          if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(C::kBVF + st), bytes);
-#pragma unroll
-          for (int p = 0; p < 8; ++p)
-            if (p < npg)
-              for (int kb = 0; kb < C::kKB; ++kb)
-                tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384 + p * rowb, &tm_v,
-                                 bar(C::kBVF + st), kb * 64, 0, zc[p], pol_kv);
-          nv = t + 1;
-        } else {
-          if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
-          for (int kb = 0; kb < C::kKB; ++kb)
-            tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
-                             bar(C::kBKF + st), kb * 64, kt * 128, kvh, pol_kv);
-          nk = t + 1;
-          if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
-          for (int kb = 0; kb < C::kKB; ++kb)
-            tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
-                             bar(C::kBVF + st), kb * 64, kt * 128, kvh, pol_kv);
-          nv = t + 1;
-        }
+        if (!mbar_wait(bar(C::kBKE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBKF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kKOff + st * C::kTileBytes + kb * 16384, &tm_k,
+                           bar(C::kBKF + st), kb * 64, kt * 128, kvh, pol_kv);
+        nk = t + 1;
+        if (!mbar_wait(bar(C::kBVE + st), ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBVF + st), C::kTileBytes);
+        for (int kb = 0; kb < C::kKB; ++kb)
+          tma_load_3d_hint(sbase + C::kVOff + st * C::kTileBytes + kb * 16384, &tm_v,
+                           bar(C::kBVF + st), kb * 64, kt * 128, kvh, pol_kv);
+        nv = t + 1;
       }
-      // paged: the last V tile's full barrier is waited here, by the thread
-      // that loaded it (its phase is unambiguous: the stage's previous phase
-      // completed before this load was issued), then handed to the zeroing warp
-      if (zero_tail && nv == n_tiles &&
-          mbar_wait(bar(C::kBVF + (n_tiles - 1) % C::kStages), ((n_tiles - 1) / C::kStages) & 1, abort_flag))
-        mbar_arrive(bar(C::kBVL));
       if (*abort_flag) {
         // let every copy still in flight land before the CTA exits
         mbar_wait_drain(bar(C::kBQ), 0, abort_flag);
@@ -303,11 +229,7 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t ph = (u / C::kStages) & 1;
         const int pb = u & 1;
         if (!mbar_wait(bar(C::kBPF + pb), (u >> 1) & 1, abort_flag)) return false;
-        if (zero_tail && u == n_tiles - 1) {
-          if (!mbar_wait(bar(C::kBVZ), 0, abort_flag)) return false;
-        } else if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) {
-          return false;
-        }
+        if (!mbar_wait(bar(C::kBVF + st), ph, abort_flag)) return false;
         tc_fence_after();
         const uint32_t vbase = sbase + C::kVOff + st * C::kTileBytes;
         const uint32_t pcol = tmem + (pb ? C::kColP1 : C::kColP0);
@@ -348,11 +270,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           // A = Q, B = K_j, both K-major: 16 head-dim elements = 32 B per step
-          // (Q's column blocks are kQColBlock bytes apart, K's 16 KB)
-          const uint32_t qoff = (ks >> 2) * C::kQColBlock + (ks & 3) * 32;
-          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + qoff, 16, 1024),
-                 sdesc_sw128(kbase + koff, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
+                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF + sb));
         mma_commit(bar(C::kBKE + st));
@@ -363,36 +283,18 @@ __global__ void __launch_bounds__(256, 1)
       mma_commit(bar(C::kBDR));
       mbar_wait_drain(bar(C::kBDR), 0, abort_flag);
     }
-  } else if (PAGED && warp == 2) {
-    // ------------------------------------------------------------ V tail
-    if (zero_tail) {
-      const int t = n_tiles - 1;
-      const int st = t % C::kStages;
-      const int valid = kvl - (t_lo + t) * 128;  // 1 .. 127 keys of the tile are real
-      if (mbar_wait_warp(bar(C::kBVL), 0, abort_flag)) {
-        // whole 128-byte rows: the swizzle only permutes 16-byte chunks within a row
-        uint8_t *vt = smem + C::kVOff + st * C::kTileBytes;
-        for (int kb = 0; kb < C::kKB; ++kb)
-          for (int i = lane; i < (128 - valid) * 8; i += 32)
-            *reinterpret_cast<uint4 *>(vt + kb * 16384 + (valid + (i >> 3)) * 128 + (i & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBVZ));
-      }
-    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int row = tid - 128;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int q_row = qt * C::kQRows + row;
+    const int q_row = qt * 128 + row;
     const float sl2 = a.scale_log2;
     // every row of this warp lies past N (the last query tile; the padding of
     // a decode block): its P rows feed only O rows that are never stored, so
     // it skips the softmax and only keeps the P barrier's count in step.
     // S(t) complete implies the P barrier's previous phase of this buffer
     // completed (S(t) overwrote S(t-2) after P(t-2) arrived).
-    const bool pad_warp = (warp & 3) * 32 >= C::kQRows || qt * C::kQRows + (warp & 3) * 32 >= a.N;
+    const bool pad_warp = qt * 128 + (warp & 3) * 32 >= a.N;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
@@ -428,7 +330,6 @@ __global__ void __launch_bounds__(256, 1)
       // mask: keys past kv_len / N, and keys after the query on the diagonal
       int limit = kvl - kt * 128;
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
-      if (PAGED) limit = (q_row < a.N) ? limit - a.dec_nq + 1 + q_row % a.dec_nq : 0;
       float m_new, alpha;
       const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
       l = l * alpha + rs;
