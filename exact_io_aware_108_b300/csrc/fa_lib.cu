@@ -313,16 +313,19 @@ int resolve_splits(long long ctas, int nkt, bool causal, int requested) {
   return best;
 }
 
-// Decode split factor: the request when it is >= 1, else the smallest S
-// that gives about 7 waves of CTAs, with at least 16 key tiles of the
-// longest sequence per share, at most 64 shares. The key walk is bound by
-// HBM: many CTAs let the block scheduler balance sequences of unequal
-// length, while short shares pay their start-up (first K/V latency) and
-// partial-result traffic too often (measured on 32 and 4 sequences of
-// 4K-8K and 16K-32K keys, page sizes 16 and 128).
+// Decode split factor: the request when it is >= 1; else, with 2 * SMs CTA
+// slots (the decode kernel runs two CTAs per SM), as many shares as fill one
+// wave of slots when that is at least 2, otherwise about two waves' worth,
+// with at least 16 key tiles of the longest sequence per share and at most
+// 64 shares. The key walk is bound by HBM; a share that is too short pays
+// its start-up (first K/V latency) and partial-result traffic too often, and
+// a partly filled last wave leaves SMs idle (measured: 4, 8, 16, 32 and 128
+// sequences of 16K-32K, 2K-8K and 1K-2K keys).
 int resolve_decode_splits(long long ctas, int nkt_max, int requested) {
   if (requested >= 1) return requested;
-  const long long want = (7 * static_cast<long long>(sm_count()) + ctas - 1) / ctas;
+  const long long slots = 2ll * sm_count();
+  const long long one_wave = slots / ctas;
+  const long long want = one_wave >= 2 ? one_wave : std::max(1ll, 2 * slots / ctas);
   const long long cap = std::max(1, std::min(64, nkt_max / 16));
   return static_cast<int>(std::max(1ll, std::min(want, cap)));
 }

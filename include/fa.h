@@ -215,9 +215,10 @@ size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
  *   h / (H / Hkv). A query with no visible key gets O = 0, LSE = -inf.
  *   page_size in {16, 32, 64, 128}; d in {64, 128}; H % Hkv == 0.
  *   num_splits, workspace: as for fa_fwd_splitkv (the key tiles of each
- *   sequence are shared by S CTAs and merged); num_splits <= 0 picks the
- *   smallest S giving about 7 waves of CTAs, with at least 16 key tiles
- *   of the longest sequence per share. The workspace size is
+ *   sequence are shared by S CTAs and merged); num_splits <= 0 picks S
+ *   to fill one wave of CTAs (two per SM) when that gives at least two
+ *   shares, else about two waves, with at least 16 key tiles of the
+ *   longest sequence per share. The workspace size is
  *   fa_decode_paged_workspace_size.
  */
 fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
