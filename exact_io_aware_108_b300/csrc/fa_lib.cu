@@ -19,6 +19,7 @@
 #include "fwd2_kernel.cuh"
 #include "fwd_fp8.cuh"
 #include "decode_kernel.cuh"
+#include "fwd_small_kernel.cuh"
 #include "bwd_kernel.cuh"
 
 namespace {
@@ -210,6 +211,45 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   return true;
 }
 
+// Short-sequence forward: one query tile per CTA, two CTAs per SM; used up
+// to this many 128-row query tiles (N <= 2048).
+constexpr int kSmallMaxTiles = 16;
+
+// Short-sequence forward: one query tile per CTA, two CTAs per SM. Like the
+// two-tile kernel it relies on setmaxnreg, so it runs only when built with
+// exactly the register count its split assumes (checked once per kernel and
+// device); returns false (nothing launched) otherwise.
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+bool try_launch_fwd_small(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const fa::FwdArgs &a, int grid, cudaStream_t st, fa_status *r) {
+  auto kern = fa::fwd_small_kernel<D, BF16, CAUSAL, SPLIT>;
+  static std::mutex mu;
+  static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (usable[dev] == 0) {
+      cudaFuncAttributes at;
+      usable[dev] = (cudaFuncGetAttributes(&at, reinterpret_cast<const void *>(kern)) == cudaSuccess &&
+                     at.numRegs == fa::SmallCfg<D>::kLaunchRegs)
+                        ? 1
+                        : -1;
+    }
+    if (usable[dev] < 0) return false;
+  }
+  constexpr int smem = fa::SmallCfg<D>::kSmemBytes;
+  cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) {
+    *r = cuda_fail(e, "cudaFuncSetAttribute(fwd small)");
+    return true;
+  }
+  kern<<<grid, 256, smem, st>>>(tq, tk, tv, a);
+  e = cudaGetLastError();
+  *r = (e != cudaSuccess) ? cuda_fail(e, "fwd small launch") : FA_OK;
+  return true;
+}
+
 // Paged decode: two CTAs per SM (128 threads, DecCfg<D>::kSmemBytes each).
 template <int D, bool BF16>
 fa_status launch_decode(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -245,10 +285,16 @@ fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if (r != FA_OK) return r;
     return launch_merge<BF16>(a, static_cast<long long>(grid / a.nqt) * a.N, D, st);
   }
+  // short sequences: one query tile per CTA, two CTAs per SM (the start-up
+  // and epilogue of one CTA overlap the other's tiles)
+  fa_status r = FA_OK;
+  if (a.nqt <= kSmallMaxTiles &&
+      (causal ? try_launch_fwd_small<D, BF16, true, SPLIT>(tq, tk, tv, a, grid, st, &r)
+              : try_launch_fwd_small<D, BF16, false, SPLIT>(tq, tk, tv, a, grid, st, &r)))
+    return r;
   // dense / causal / key padding: two query tiles per CTA
   const long long bh = grid / a.nqt;
   const int grid2 = static_cast<int>(bh * ((a.nqt + 1) / 2));
-  fa_status r = FA_OK;
   if (causal ? try_launch_fwd2<D, BF16, true, SPLIT>(tq, tk, tv, a, grid2, st, &r)
              : try_launch_fwd2<D, BF16, false, SPLIT>(tq, tk, tv, a, grid2, st, &r))
     return r;
