@@ -212,8 +212,13 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 }
 
 // Short-sequence forward: one query tile per CTA, two CTAs per SM; used up
-// to this many 128-row query tiles (N <= 2048).
+// to this many 128-row query tiles (N <= 2048), and at any length when the
+// two-tile kernel's grid (one CTA per pair of query tiles) would leave SMs
+// idle: it then runs twice as many CTAs (measured: one head of N = 8192,
+// 344 against 263 TFLOP/s; with 128 heads of N = 4096 the two-tile kernel
+// stays ahead, 1043 against 1016).
 constexpr int kSmallMaxTiles = 16;
+int sm_count();
 
 // Short-sequence forward: one query tile per CTA, two CTAs per SM. Like the
 // two-tile kernel it relies on setmaxnreg, so it runs only when built with
@@ -288,7 +293,7 @@ fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   // short sequences: one query tile per CTA, two CTAs per SM (the start-up
   // and epilogue of one CTA overlap the other's tiles)
   fa_status r = FA_OK;
-  if (a.nqt <= kSmallMaxTiles &&
+  if ((a.nqt <= kSmallMaxTiles || (grid / a.nqt) * ((a.nqt + 1) / 2) < sm_count()) &&
       (causal ? try_launch_fwd_small<D, BF16, true, SPLIT>(tq, tk, tv, a, grid, st, &r)
               : try_launch_fwd_small<D, BF16, false, SPLIT>(tq, tk, tv, a, grid, st, &r)))
     return r;

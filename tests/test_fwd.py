@@ -179,6 +179,30 @@ def test_fwd_full_size_sampled(name):
     check(f"LSE[{b},{h}] whole head", lse[b, h], lse_ref[0, 0], TOL_LSE, torch.float32)
 
 
+@pytest.mark.parametrize("B,H,N,d,dt,causal", [
+    (1, 1, 3000, 128, "bf16", True),    # 24 query tiles, 12 pairs: a grid of fewer CTAs than SMs
+    (1, 2, 4500, 64, "f16", False),     # 36 query tiles with a ragged tail
+])
+def test_fwd_few_heads_long_sequence(B, H, N, d, dt, causal):
+    """Few heads of a long sequence run the one-tile-per-CTA forward (the
+    two-tile grid would leave SMs idle): every element against the oracle,
+    with and without O's residual."""
+    import exact_io_aware_108_b300 as fa
+    t = inputs.make_qkv(B, H, N, d, dt, seed=N + H, with_dout=False)
+    q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_forward(q, k, v, scale, causal=causal)
+    o2, lse2, o_res = fa.attention_forward(q, k, v, scale, causal=causal, return_residual=True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+    o_ref, lse_ref = ref.attn_fwd(t["q"], t["k"], t["v"], scale, causal)
+    check("O", o.cpu(), o_ref, TOL_O, q.dtype)
+    check("LSE", lse.cpu(), lse_ref, TOL_LSE, torch.float32)
+    check("O (residual path)", o2.cpu(), o_ref, TOL_O, q.dtype)
+    o32 = o2.cpu().double().numpy() + o_res.cpu().double().numpy()
+    assert np.max(np.abs(o32 - o_ref)) < 2e-3
+
+
 @pytest.mark.parametrize("d,dt", [(128, "bf16"), (64, "f16")])
 def test_fwd_residual_path_is_accurate(d, dt):
     """With o_res requested the forward feeds P to the tensor core as a
