@@ -29,8 +29,10 @@ from ._binding import (  # noqa: F401
     fa_fwd_splitkv,
     fa_fwd_splitkv_num_splits,
     fa_fwd_splitkv_workspace_size,
+    fa_debug_starve_pipelines,
     fa_get_device_error,
     fa_last_error_message,
+    fa_set_wait_limit_ns,
     fa_status_str,
     fa_version,
     exported_symbols,

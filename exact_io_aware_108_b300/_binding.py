@@ -23,7 +23,8 @@ EXPORTS = (
     "fa_decode_paged", "fa_decode_paged_num_splits", "fa_decode_paged_workspace_size", "fa_bwd",
     "fa_bwd_gqa", "fa_bwd_blocksparse", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace",
-    "fa_get_device_error", "fa_status_str", "fa_last_error_message", "fa_version",
+    "fa_get_device_error", "fa_set_wait_limit_ns", "fa_debug_starve_pipelines", "fa_status_str",
+    "fa_last_error_message", "fa_version",
 )
 
 _lock = threading.Lock()
@@ -95,6 +96,8 @@ def load_library():
         lib.fa_bwd_noalloc_max_workspace.argtypes = []
         lib.fa_bwd_noalloc_max_workspace.restype = _sz
         lib.fa_get_device_error.argtypes = [_vp]
+        lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_debug_starve_pipelines.argtypes = [_i]
         lib.fa_status_str.argtypes = [_i]
         lib.fa_status_str.restype = ctypes.c_char_p
         lib.fa_last_error_message.argtypes = []
@@ -105,7 +108,8 @@ def load_library():
                      "fa_decode_paged", "fa_bwd",
                      "fa_bwd_gqa",
                      "fa_bwd_blocksparse",
-                     "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error"):
+                     "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish", "fa_get_device_error",
+                     "fa_set_wait_limit_ns", "fa_debug_starve_pipelines"):
             getattr(lib, name).restype = _i
         _lib = lib
         return lib
@@ -345,6 +349,16 @@ def fa_bwd_noalloc_max_workspace() -> int:
 def fa_get_device_error(stream=None) -> int:
     """Synchronise the stream and return the device error status (0 = FA_OK)."""
     return int(load_library().fa_get_device_error(_stream(stream)))
+
+
+def fa_set_wait_limit_ns(ns: int) -> int:
+    """Time limit of the kernels' pipeline waits (0 = the 2 s default)."""
+    return int(load_library().fa_set_wait_limit_ns(int(ns)))
+
+
+def fa_debug_starve_pipelines(enable: bool) -> int:
+    """Test switch: the kernels' load-issuing threads issue nothing."""
+    return int(load_library().fa_debug_starve_pipelines(1 if enable else 0))
 
 
 def fa_status_str(status: int) -> str:

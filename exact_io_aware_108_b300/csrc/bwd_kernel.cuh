@@ -8,20 +8,43 @@
 //   dS    = P o (dP - D_i),     D_i = rowsum(dO_i o O_i)
 //   dK_j += scale dS^T Q_i      dQ_i += scale dS K_j
 //
-// Three kernels:
+// Precision. All five products take fp16 operands, whatever the input type:
+// P and dS are rounded to fp16 (11 significant bits) before their products,
+// not to bf16 (8 bits). With sharp bf16 softmax at d = 128 (logit std 4) the
+// bf16 rounding of dS alone puts rare dQ and dK elements past a 2e-2
+// absolute error (dS rows sum to zero, so a dQ element can be much smaller
+// than the terms whose rounding errors it collects). For bf16 inputs the
+// operands are converted to fp16:
+//   Q, K, V   unscaled. The conversion is exact for 2^-17 <= |x| <= 65504
+//             (smaller values are rounded to fp16's subnormal grid, an
+//             absolute change of at most 2^-25); larger values are clamped
+//             to 65504 and reported through the device error word.
+//   dO        scaled by 2^-e_do, e_do chosen from max |dO| so that the
+//             largest element lands in [2^14, 2^15): gradients of any
+//             magnitude keep fp16's full precision. dP and dV are
+//             multiplied back by 2^e_do in fp32 (exact).
+//   dS        stored as dS * scale * 2^-e_s, e_s chosen per CTA from the
+//             bound |dS| <= |dP| + |D| <= d max|dO| max|V_j| + max|D| so the
+//             largest possible value stays below 2^15; dQ and dK partials are
+//             multiplied back by 2^e_s in fp32 (exact).
+// For fp16 inputs only the dS scaling applies.
+//
+// Kernels:
 //   bwd_pre_kernel   -scale * D_i and -LSE_i * log2(e) per query row (padded
 //                    to whole 128-row tiles; pad rows get D = 0, LSE = +inf so
-//                    P = 0)
-//                    and zeroes the fp32 dQ accumulator. D_i = dO_i . O_i
-//                    uses O plus its rounding residual when the forward
-//                    wrote one: with bf16 O alone the rounding of O moves
-//                    D_i by up to ~0.05 at d = 128, which reaches dQ and dK.
+//                    P = 0), zeroes the fp32 dQ accumulator, and records
+//                    max |dO| and max |D| for the scaling above. D_i = dO_i .
+//                    O_i uses O plus its rounding residual when the forward
+//                    wrote one: with bf16 O alone the rounding of O moves D_i
+//                    by up to ~0.05 at d = 128, which reaches dQ and dK.
+//   bwd_cvt_kernel   (bf16 inputs) Q -> fp16 and dO -> fp16 * 2^-e_do into
+//                    the workspace, read by the main kernel's tensor maps.
 //   bwd_main_kernel  one CTA per 128-key tile of one (batch, key/value head);
-//                    K_j, V_j stay in shared memory, dK_j and dV_j stay in
-//                    TMEM, and the CTA loops over the query tiles that see
-//                    key tile j, of every query head that reads this
-//                    key/value head (one head unless the attention is
-//                    grouped-query).
+//                    K_j, V_j stay in shared memory (converted there to fp16
+//                    for bf16 inputs), dK_j and dV_j stay in TMEM, and the
+//                    CTA loops over the query tiles that see key tile j, of
+//                    every query head that reads this key/value head (one
+//                    head unless the attention is grouped-query).
 //                    The scores are computed transposed (keys on TMEM lanes)
 //                    so P^T and dS^T are row-local to one thread per key.
 //   bwd_dq_kernel    dQ accumulator (fp32) -> dQ (fp16/bf16).
@@ -31,16 +54,19 @@
 //   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
 //                   query tile i through a two-stage ring.
 //   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
+//   warpgroups 1-3  at the start: K_j, V_j -> fp16 in place (bf16 inputs),
+//                   max |V_j| and e_s.
 //   warpgroups 1, 2 one 64-query half h of the tile each: P^T -> TMEM
-//                   (16-bit), dS^T -> shared memory (16-bit, scale folded
-//                   in, computed from the fp32 P). A thread holds 4 keys x
-//                   16 queries (16-lane TMEM shapes), so it reads only 16 of
-//                   the half's per-query LSE and D values; at the end
+//                   (fp16), dS^T -> shared memory (fp16, scale and 2^-e_s
+//                   folded in, computed from the fp32 P). A thread holds 4
+//                   keys x 16 queries (16-lane TMEM shapes), so it reads only
+//                   16 of the half's per-query LSE and D values; at the end
 //                   warpgroup 1 writes dK, warpgroup 2 writes dV (one key
 //                   row per thread).
-//   warpgroup 3     reads the dQ partial from TMEM and adds it to the fp32
-//                   accumulator (d = 128: thread r owns head-dim channel r of
-//                   the transposed partial; d = 64: thread r owns query r).
+//   warpgroup 3     reads the dQ partial from TMEM and adds it, times 2^e_s,
+//                   to the fp32 accumulator (d = 128: thread r owns head-dim
+//                   channel r of the transposed partial; d = 64: thread r
+//                   owns query r).
 // The MMA issue order per query tile i is dP_i, dV_i, dQ_i, S_{i+1}, dK_i
 // for d = 128: the next score tile is computed before dK_i, so the P phase
 // of tile i+1 overlaps the dK_i product and the dQ_i read-out, while the Q
@@ -65,6 +91,13 @@ struct BwdArgs {
   float *dq_acc;    // [BH, nqt*128, D]
   const int32_t *kv_len;
   const uint8_t *block_mask;
+  // bf16 inputs: the fp16 copies of Q and of dO * 2^-e_do ([B*H, N, D],
+  // written by bwd_cvt_kernel) and the sources they are made from
+  const void *q;
+  void *q16, *do16;
+  // [0] max |dO| and [1] max |D| as fp32 bit patterns (non-negative floats
+  // order like their bits), zeroed before bwd_pre_kernel
+  unsigned int *stats;
   int H, N, nqt, nkt;
   int hgroup;    // heads per scheduling group (causal launch order, see below)
   int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
@@ -85,16 +118,74 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// 2^e as an fp32 value, e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// e such that x * 2^-e lies in [2^(top-1), 2^top) for finite x > 0; 0
+// otherwise. Clamped to [-120, 120] so both 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int scale_exponent(float x, int top) {
+  if (!(x > 0.f) || !(x <= 3.0e38f)) return 0;
+  int e;
+  frexpf(x, &e);  // x = m 2^e, m in [0.5, 1): x < 2^e
+  e -= top;
+  return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+
+// Exponent of the dO scaling: max |dO| * 2^-e_do in [2^14, 2^15).
+__device__ __forceinline__ int do_exponent(const unsigned int *stats) {
+  return scale_exponent(__uint_as_float(stats[0]), 15);
+}
+
+// Eight bf16 values (16 bytes) -> eight fp16 values, rounded to nearest and
+// clamped to +-65504; amax takes the largest magnitude seen.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, float &amax) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lo = __uint_as_float(in[k] << 16), hi = __uint_as_float(in[k] & 0xFFFF0000u);
+    amax = fmax3(amax, fabsf(lo), fabsf(hi));
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(out[k]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Largest magnitude of eight 16-bit values.
+template <bool BF16>
+__device__ __forceinline__ float amax16x8(uint4 w) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m = fmax3(m, fabsf(unpack_lo<BF16>(in[k])), fabsf(unpack_hi<BF16>(in[k])));
+  return m;
+}
+
+// Block-wide max of a non-negative value, then one atomicMax on its bits.
+__device__ __forceinline__ void block_max_to(unsigned int *dst, float v, float *red) {
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, s));
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
+    atomicMax(dst, __float_as_uint(m));
+  }
+}
+
 // ----------------------------------------------------------------- pre
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long rows_pad) {
   constexpr int LPR = D / 8;         // lanes per row (8 elements each)
   constexpr int RPW = 32 / LPR;      // rows per warp step
+  __shared__ float red[2][8];
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR, grp = lane / LPR;
   const long long tile_rows = static_cast<long long>(a.nqt) * 128;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  float amax_do = 0.f, amax_d = 0.f;
   for (long long base = w0 * RPW; base < rows_pad; base += warps * RPW) {
     const long long row = base + grp;
     const bool live = row < rows_pad;
@@ -119,6 +210,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
           acc = fmaf(unpack_lo<BF16>(ow[k]) + unpack_lo<BF16>(rw[k]), unpack_lo<BF16>(gw[k]), acc);
           acc = fmaf(unpack_hi<BF16>(ow[k]) + unpack_hi<BF16>(rw[k]), unpack_hi<BF16>(gw[k]), acc);
         }
+        amax_do = fmaxf(amax_do, amax16x8<BF16>(g4));
       }
       float4 *z = reinterpret_cast<float4 *>(a.dq_acc + row * D + sub * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -131,6 +223,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
       // P = 2^(s * scale * log2 e + nl) and dS = P * (dP * scale + nd)
       // with one packed FMA per pair
       a.delta[row] = -a.scale * acc;
+      amax_d = fmaxf(amax_d, fabsf(acc));
       float nl = -INFINITY;
       if (i < a.N) {
         const float l = a.lse[static_cast<size_t>(bh) * a.N + i];
@@ -139,6 +232,31 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
       a.lse_l2[row] = nl;
     }
   }
+  block_max_to(a.stats + 0, amax_do, red[0]);
+  block_max_to(a.stats + 1, amax_d, red[1]);
+}
+
+// ----------------------------------------------------------------- fp16 copies
+// bf16 inputs: Q -> fp16 (unscaled) and dO -> fp16 * 2^-e_do, 16 bytes per
+// thread step, grid-stride over [B*H, N, D] (n16 groups of 8 elements).
+__global__ void __launch_bounds__(256) bwd_cvt_kernel(const BwdArgs a, long long n16) {
+  const float f_do = exp2i(-do_exponent(a.stats));
+  float amax_q = 0.f;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n16;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 q = reinterpret_cast<const uint4 *>(a.q)[g];
+    reinterpret_cast<uint4 *>(a.q16)[g] = bf16x8_to_f16x8(q, amax_q);
+    const uint4 w = reinterpret_cast<const uint4 *>(a.dout)[g];
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(in[k] << 16) * f_do, hi = __uint_as_float(in[k] & 0xFFFF0000u) * f_do;
+      asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(out[k]) : "f"(hi), "f"(lo));
+    }
+    reinterpret_cast<uint4 *>(a.do16)[g] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  if (amax_q > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
 }
 
 // ----------------------------------------------------------------- dq convert
@@ -174,14 +292,16 @@ struct BwdCfg {
   static constexpr int kBarOff = kDeltaOff + 1024;
   static constexpr int kBKV = 0, kBQF = 1, kBQE = 3, kBSF = 5, kBDPF = 6, kBPR = 7 /* x2 */,
                        kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13, kBDSF = 14,
-                       kNumBars = 15;
+                       kBCV = 15 /* K, V ready in fp16, 384 arrivals */, kNumBars = 16;
   // d = 128: the dQ partial is computed transposed (dQ^T = K^T dS^T, TMEM
   // lane = head-dim channel, column = query) so one warp's reduction into
   // the fp32 accumulator covers 32 consecutive channels of a row: a whole
   // 128-byte line per instruction instead of 32 scattered 16-byte pieces.
   static constexpr bool kDqT = (D == 128);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16;
+  // misc: [0] TMEM address, [1] abort flag, [4, 16) per-warp max |V| of
+  // warpgroups 1-3 (fp32)
+  static constexpr int kSmemBytes = kMiscOff + 64;
   static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr uint32_t kColDQ = kDqT ? kColDP : 2 * D + 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -214,7 +334,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (sbase & 1023u) {  // the swizzled tiles need a 1 KB aligned base
-    if (tid == 0) atomicOr(&g_fa_device_error, kDevErrTimeout);
+    if (tid == 0) atomicOr(&g_fa_device_error, kDevErrSmemAlign);
     return;
   }
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
@@ -278,6 +398,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(C::kBDQE), 128);
     mbar_init(bar(C::kBFIN), 1);
     mbar_init(bar(C::kBDSF), 1);
+    mbar_init(bar(C::kBCV), 384);
     *abort_flag = 0u;
     fence_barrier_init();
     prefetch_tensormap(&tm_q);
@@ -299,7 +420,7 @@ __global__ void __launch_bounds__(512, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0 && n_iter > 0 && !pipelines_starved()) {
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBKV), 2 * C::kTileBytes);
@@ -334,10 +455,11 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t kIdSS = idesc_f16(BF16, 128, 128, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_f16(BF16, 128, D, false, true);      // dK, dV
-      constexpr uint32_t kIdQ = C::kDqT ? idesc_f16(BF16, 128, 128, true, true)  // dQ^T
-                                        : idesc_f16(BF16, 128, D, true, true);   // dQ
+      // every operand is fp16 (bf16 inputs are converted; see the top)
+      constexpr uint32_t kIdSS = idesc_f16(false, 128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdKV = idesc_f16(false, 128, D, false, true);      // dK, dV
+      constexpr uint32_t kIdQ = C::kDqT ? idesc_f16(false, 128, 128, true, true)  // dQ^T
+                                        : idesc_f16(false, 128, D, true, true);   // dQ
       // S^T = K_j Q_i^T for the query tile in stage st
       auto issue_s = [&](int st) {
         const uint32_t sb = opaque_u32(sbase);
@@ -350,7 +472,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(bar(C::kBSF));
       };
-      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
+      bool ok = mbar_wait(bar(C::kBCV), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -439,12 +561,54 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // ---- prologue of warpgroups 1-3: K_j, V_j -> fp16 in place (bf16
+    // inputs), max |V_j| per warp into shared memory
+    float *slots = reinterpret_cast<float *>(misc + 4);
+    if (n_iter > 0) {
+      float amax_v = 0.f, amax_k = 0.f;
+      if (mbar_wait_warp(bar(C::kBKV), 0, abort_flag)) {
+        constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
+        uint4 *kv = reinterpret_cast<uint4 *>(smem + C::kKOff);  // K then V (adjacent)
+        static_assert(C::kVOff == C::kKOff + C::kTileBytes, "K and V tiles are adjacent");
+        for (int c = tid - 128; c < 2 * kChunks; c += 384) {
+          const uint4 w = kv[c];
+          if constexpr (BF16) {
+            float m = 0.f;
+            kv[c] = bf16x8_to_f16x8(w, m);
+            if (c < kChunks) amax_k = fmaxf(amax_k, m); else amax_v = fmaxf(amax_v, m);
+          } else if (c >= kChunks) {
+            amax_v = fmaxf(amax_v, amax16x8<false>(w));
+          }
+        }
+        if (BF16 && fmaxf(amax_k, amax_v) > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
+        if (BF16) fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kBCV));
+#pragma unroll
+      for (int s2 = 16; s2 > 0; s2 >>= 1) amax_v = fmaxf(amax_v, __shfl_xor_sync(0xffffffffu, amax_v, s2));
+      if (lane == 0) slots[warp - 4] = amax_v;
+      named_bar_sync(2, 384);
+    }
+    // e_s: |dS| <= |dP| + |D| <= d max|dO| max|V_j| + max|D| (clamped values
+    // are at most 65504, so the bound stays finite for finite inputs); dS is
+    // stored times scale 2^-e_s. e_do: dO16 = dO 2^-e_do.
+    auto exponent_s = [&]() -> int {
+      float amax_v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 12; ++w) amax_v = fmaxf(amax_v, slots[w]);
+      const float amax_do = __uint_as_float(a.stats[0]), amax_d = __uint_as_float(a.stats[1]);
+      return scale_exponent(a.scale * (static_cast<float>(D) * amax_do * fminf(amax_v, 65504.f) + amax_d), 15);
+    };
+    auto exponent_do = [&]() -> int { return BF16 ? do_exponent(a.stats) : 0; };
     if (warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T, one query half
     const int h = (warp >> 2) - 1;  // query half: columns [64h, 64h+64) of the tile
     const int r = tid & 127;         // key row of this thread's lane (epilogue)
     const int key = kt * 128 + r;
-    const float sl2 = a.scale_log2, scale = a.scale;
+    const float sl2 = a.scale_log2;
+    const float f_s = n_iter > 0 ? exp2i(-exponent_s()) : 1.f;
+    const float sc_dp = a.scale * f_s * exp2i(exponent_do());
     // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
     // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
     // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
@@ -512,8 +676,8 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t w[16];
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          w[2 * b] = pack2<BF16>(p[j][4 * b], p[j][4 * b + 1]);
-          w[2 * b + 1] = pack2<BF16>(p[j][4 * b + 2], p[j][4 * b + 3]);
+          w[2 * b] = pack2<false>(p[j][4 * b], p[j][4 * b + 1]);
+          w[2 * b + 1] = pack2<false>(p[j][4 * b + 2], p[j][4 * b + 3]);
         }
         tmem_st_16x128b_x8(tq + (static_cast<uint32_t>(16 * j) << 16) + C::kColS + 64 * h, w);
       }
@@ -532,15 +696,16 @@ __global__ void __launch_bounds__(512, 1)
       reg_fence_32(dv[1]);
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
-        const float2 nd = nd2[4 * b];
+        float2 nd = nd2[4 * b];
+        fmul2(nd.x, nd.y, nd.x, nd.y, f_s, f_s);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            // dS = P * (dP * scale - scale * D), scale folded in for dK and dQ
+            // dS * scale * 2^-e_s = P * (dP16 * scale * 2^(e_do - e_s) - scale * D * 2^-e_s)
             const int e = 4 * b + 2 * i;
             float t0, t1;
-            ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), scale, scale, nd.x,
+            ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), sc_dp, sc_dp, nd.x,
                   nd.y);
             fmul2(t0, t1, t0, t1, p[j][e], p[j][e + 1]);
             // row = key of the dS^T tile; queries 8b + 2c4, +1 are the 4-byte
@@ -548,7 +713,7 @@ __global__ void __launch_bounds__(512, 1)
             // swizzled by (row & 7) = t4
             const int row = 32 * (warp & 3) + 16 * j + 8 * i + t4;
             const uint32_t addr = sDS + row * 128 + ((b ^ t4) << 4) + 4 * c4;
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<BF16>(t0, t1)) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<false>(t0, t1)) : "memory");
           }
       }
       fence_proxy_async_smem();
@@ -579,20 +744,24 @@ __global__ void __launch_bounds__(512, 1)
         for (int i = 0; i < 32; ++i) v[j][i] = 0u;
     }
     if (key < a.N) {
+      // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO)
+      const float u = exp2i(h == 0 ? (n_iter > 0 ? exponent_s() : 0) : exponent_do());
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
+        float f[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) fmul2(f[i], f[i + 1], __uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]), u, u);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack2<BF16>(__uint_as_float(v[j][8 * q]), __uint_as_float(v[j][8 * q + 1])),
-                             pack2<BF16>(__uint_as_float(v[j][8 * q + 2]), __uint_as_float(v[j][8 * q + 3])),
-                             pack2<BF16>(__uint_as_float(v[j][8 * q + 4]), __uint_as_float(v[j][8 * q + 5])),
-                             pack2<BF16>(__uint_as_float(v[j][8 * q + 6]), __uint_as_float(v[j][8 * q + 7])));
+          d4[q] = make_uint4(pack2<BF16>(f[8 * q], f[8 * q + 1]), pack2<BF16>(f[8 * q + 2], f[8 * q + 3]),
+                             pack2<BF16>(f[8 * q + 4], f[8 * q + 5]), pack2<BF16>(f[8 * q + 6], f[8 * q + 7]));
       }
     }
     } else {
     // ------------------------------------------------------------ dQ partials
     const int r = tid & 127;  // d = 128: head-dim channel; d = 64: query row
+    const float u_s = n_iter > 0 ? exp2i(exponent_s()) : 1.f;  // the partial carries 2^-e_s
     int g = 0, qi = q_first;
     for (int u = 0; u < n_iter; ++u) {
       if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
@@ -620,7 +789,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int j = 0; j < 4; ++j)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]));
+            atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]) * u_s);
             if ((i & 15) == 15) {
               const long long t0 = clock64();
               while (clock64() - t0 < 120) {
@@ -634,8 +803,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             atomicAdd(reinterpret_cast<float4 *>(acc + j * 32 + i),
-                      make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
-                                  __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
+                      make_float4(__uint_as_float(v[j][i]) * u_s, __uint_as_float(v[j][i + 1]) * u_s,
+                                  __uint_as_float(v[j][i + 2]) * u_s, __uint_as_float(v[j][i + 3]) * u_s));
       }
       advance(g, qi);
     }

@@ -6,9 +6,28 @@
 namespace fa {
 
 // A pipeline wait that takes longer than this is a bug; the kernel gives up.
+// g_fa_wait_limit_ns holds the limit the kernels use (the host may lower it,
+// fa_set_wait_limit_ns); waits that drain copies already in flight after an
+// abort always allow kWaitLimitNs, so those copies land before the CTA exits.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ unsigned long long g_fa_wait_limit_ns = kWaitLimitNs;
 
-enum : uint32_t { kDevErrTimeout = 1u };
+// Nonzero: the TMA producer of every attention kernel issues no loads, so
+// each CTA's first pipeline wait can only end by running out of time. Set by
+// fa_debug_starve_pipelines to exercise the time limit, the abort flag and
+// the device error word; zero in normal operation.
+__device__ unsigned int g_fa_starve_pipelines = 0;
+__device__ __forceinline__ bool pipelines_starved() {
+  return *static_cast<volatile unsigned int *>(&g_fa_starve_pipelines) != 0u;
+}
+
+// Bits of the device error word.
+//   kDevErrTimeout    a pipeline wait ran out of time
+//   kDevErrSmemAlign  the dynamic shared-memory base was not 1 KB aligned
+//                     (the kernel returned before doing any work)
+//   kDevErrRange      a bf16 input value that the backward converts to fp16
+//                     was beyond fp16's largest finite value, 65504
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrSmemAlign = 2u, kDevErrRange = 4u };
 
 // Device error word, read and cleared by fa_get_device_error(). Kernels and
 // the host code that reads it live in one translation unit (fa_lib.cu).
@@ -22,11 +41,13 @@ __device__ unsigned int g_fa_device_error = 0;
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             volatile uint32_t *abort_flag, bool honor_abort) {
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit =
+      honor_abort ? *static_cast<volatile unsigned long long *>(&g_fa_wait_limit_ns) : kWaitLimitNs;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 127u) == 0) {
       if (honor_abort && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit) {
         *abort_flag = 1u;
         atomicOr(&g_fa_device_error, kDevErrTimeout);
         return false;

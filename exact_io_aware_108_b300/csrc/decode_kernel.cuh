@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(128, 2)
 
   if (warp == 2) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_tiles > 0 && !pipelines_starved()) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_first();  // every cache page is read once
       mbar_arrive_expect_tx(bar(C::kBQ), C::kQBytes);
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(128, 2)
       const int kt = t_lo + t;
       const int limit = (q_row < a.N) ? kvl - kt * 128 - a.dec_nq + 1 + q_row % a.dec_nq : 0;
       float m_new, alpha;
-      const float nm = softmax_max<false>(s, limit, sl2, m, m_new, alpha);
+      const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
       // S(t) complete implies P(t-1) V(t-1) is done (S(t) waited for it): O
       // is final for tile t - 1 and can be rescaled
       if (t > 0 && __any_sync(0xffffffffu, m_new != m)) {
@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(128, 2)
       softmax_exp<0, 128>(s, sl2, nm, acc);
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t hi[16], lo[16];
-        pack_p32<BF16, false>(s, c0, hi, lo);
+        uint32_t hi[16];
+        pack_p32<BF16>(s, c0, hi);
         tmem_st_32x32b_x16(scol + c0 / 2, hi);
       }
       tmem_wait_st();

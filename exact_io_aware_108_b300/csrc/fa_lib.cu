@@ -162,10 +162,10 @@ cudaError_t set_smem(const void *kernel, int bytes) {
   return e;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
 fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, cudaStream_t st) {
-  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE, SPLIT>;
+  auto kern = fa::fwd_kernel<D, BF16, CAUSAL, SPARSE>;
   constexpr int smem = fa::FwdCfg<D>::kSmemBytes;
   cudaError_t e = set_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
@@ -179,10 +179,10 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 // warpgroups, which is only safe when the kernel was built with exactly the
 // register count the split assumes (checked once per kernel and device).
 // Returns false (nothing launched) when that check fails.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
+template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                      const fa::FwdArgs &a, int nqb_grid, cudaStream_t st, fa_status *r) {
-  auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, SPLIT, FP8>;
+  auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, FP8>;
   using C2 = fa::Fwd2Cfg<D, FP8>;
   static std::mutex mu;
   static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
@@ -224,10 +224,10 @@ int sm_count();
 // two-tile kernel it relies on setmaxnreg, so it runs only when built with
 // exactly the register count its split assumes (checked once per kernel and
 // device); returns false (nothing launched) otherwise.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL>
 bool try_launch_fwd_small(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const fa::FwdArgs &a, int grid, cudaStream_t st, fa_status *r) {
-  auto kern = fa::fwd_small_kernel<D, BF16, CAUSAL, SPLIT>;
+  auto kern = fa::fwd_small_kernel<D, BF16, CAUSAL>;
   static std::mutex mu;
   static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
   int dev = 0;
@@ -279,14 +279,14 @@ fa_status launch_merge(const fa::FwdArgs &a, long long rows, int d, cudaStream_t
   return e != cudaSuccess ? cuda_fail(e, "split-KV merge launch") : FA_OK;
 }
 
-template <int D, bool BF16, bool SPLIT>
-fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+template <int D, bool BF16>
+fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
-  if (sparse) return launch_fwd_t<D, BF16, false, true, SPLIT>(tq, tk, tv, a, grid, st);
+  if (sparse) return launch_fwd_t<D, BF16, false, true>(tq, tk, tv, a, grid, st);
   if (a.num_splits > 1) {
     // split-KV: single-tile kernel over (query tile, split), then the merge
-    const fa_status r = causal ? launch_fwd_t<D, BF16, true, false, SPLIT>(tq, tk, tv, a, grid, st)
-                               : launch_fwd_t<D, BF16, false, false, SPLIT>(tq, tk, tv, a, grid, st);
+    const fa_status r = causal ? launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st)
+                               : launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
     if (r != FA_OK) return r;
     return launch_merge<BF16>(a, static_cast<long long>(grid / a.nqt) * a.N, D, st);
   }
@@ -294,27 +294,19 @@ fa_status launch_fwd_s(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   // and epilogue of one CTA overlap the other's tiles)
   fa_status r = FA_OK;
   if ((a.nqt <= kSmallMaxTiles || (grid / a.nqt) * ((a.nqt + 1) / 2) < sm_count()) &&
-      (causal ? try_launch_fwd_small<D, BF16, true, SPLIT>(tq, tk, tv, a, grid, st, &r)
-              : try_launch_fwd_small<D, BF16, false, SPLIT>(tq, tk, tv, a, grid, st, &r)))
+      (causal ? try_launch_fwd_small<D, BF16, true>(tq, tk, tv, a, grid, st, &r)
+              : try_launch_fwd_small<D, BF16, false>(tq, tk, tv, a, grid, st, &r)))
     return r;
   // dense / causal / key padding: two query tiles per CTA
   const long long bh = grid / a.nqt;
   const int grid2 = static_cast<int>(bh * ((a.nqt + 1) / 2));
-  if (causal ? try_launch_fwd2<D, BF16, true, SPLIT>(tq, tk, tv, a, grid2, st, &r)
-             : try_launch_fwd2<D, BF16, false, SPLIT>(tq, tk, tv, a, grid2, st, &r))
+  if (causal ? try_launch_fwd2<D, BF16, true>(tq, tk, tv, a, grid2, st, &r)
+             : try_launch_fwd2<D, BF16, false>(tq, tk, tv, a, grid2, st, &r))
     return r;
-  if (causal) return launch_fwd_t<D, BF16, true, false, SPLIT>(tq, tk, tv, a, grid, st);
-  return launch_fwd_t<D, BF16, false, false, SPLIT>(tq, tk, tv, a, grid, st);
+  if (causal) return launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st);
+  return launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
 }
 
-// The residual path (o_res given) also runs the split-probability P V
-// product, so that O, and with it D in the backward, is accurate.
-template <int D, bool BF16>
-fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
-  if (a.o_res != nullptr) return launch_fwd_s<D, BF16, true>(tq, tk, tv, a, grid, causal, sparse, st);
-  return launch_fwd_s<D, BF16, false>(tq, tk, tv, a, grid, causal, sparse, st);
-}
 
 // Hkv: key/value heads (0 = H); H must be a multiple of it (grouped-query
 // attention: query head h reads key/value head h / (H / Hkv)).
@@ -461,9 +453,13 @@ size_t padded_rows(int B, int H, int N) {
 }
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Then a 256-byte block of statistics (max |dO|, max |D|) and, for bf16
+// inputs, the fp16 copies of Q and of the scaled dO ([B, H, N, d] each; the
+// space is reserved for either input type).
 size_t fa_bwd_ws_bytes(int B, int H, int N, int d) {
   const size_t rows = padded_rows(B, H, N);
-  return 2 * up256(rows * 4) + up256(rows * static_cast<size_t>(d) * 4);
+  const size_t elems = static_cast<size_t>(B) * H * static_cast<size_t>(N) * d;
+  return 2 * up256(rows * 4) + up256(rows * static_cast<size_t>(d) * 4) + 256 + 2 * up256(elems * 2);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool SPARSE>
@@ -507,6 +503,8 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        cudaStream_t st) {
   cudaError_t e;
   if (phases & kPrepare) {
+    e = cudaMemsetAsync(a.stats, 0, 2 * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd statistics reset");
     constexpr int rows_per_block = 8 * (32 / (D / 8));
     long long pre_blocks = (rows_pad + rows_per_block - 1) / rows_per_block;
     if (pre_blocks > 148 * 16) pre_blocks = 148 * 16;
@@ -516,6 +514,15 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   }
   if (phases & kMain) {
     fa_status r;
+    if (BF16) {
+      // fp16 copies of Q and of dO * 2^-e_do for the main kernel's products
+      const long long n16 = n_vec4 / 2;
+      long long cvt_blocks = (n16 + 255) / 256;
+      if (cvt_blocks > 148 * 16) cvt_blocks = 148 * 16;
+      fa::bwd_cvt_kernel<<<static_cast<int>(cvt_blocks), 256, 0, st>>>(a, n16);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "bwd conversion launch");
+    }
     if (sparse)
       r = launch_bwd_main_t<D, BF16, false, true>(tq, tk, tv, tdo, a, grid, st);
     else if (causal)
@@ -565,19 +572,32 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   if (ws_bytes < need)
     return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, need);
   if (sparse && block_mask == nullptr) return fail(FA_ERR_INVALID_ARG, "block_mask is null");
+  // no forward computes block-sparse attention with key padding, so its
+  // gradient is not offered either
+  if (sparse && kv_len != nullptr)
+    return fail(FA_ERR_INVALID_ARG, "kv_len cannot be combined with a block mask");
   if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
     return fail(FA_ERR_INVALID_ARG, "kv_len is not 4-byte aligned");
   if (o_res != nullptr && !aligned16(o_res))
     return fail(FA_ERR_INVALID_ARG, "o_res is not 16-byte aligned");
+  const size_t rows = padded_rows(B, H, N);
+  const size_t elems = static_cast<size_t>(s.BH) * static_cast<size_t>(N) * d;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  unsigned int *stats =
+      reinterpret_cast<unsigned int *>(ws + 2 * up256(rows * 4) + up256(rows * static_cast<size_t>(d) * 4));
+  void *q16 = reinterpret_cast<uint8_t *>(stats) + 256;
+  void *do16 = static_cast<uint8_t *>(q16) + up256(elems * 2);
   CUtensorMap tq, tk, tv, tdo;
   if (phases & kMain) {
-    if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
+    // bf16 inputs: the products read the fp16 copies of Q and dO (K and V
+    // are converted in shared memory)
+    const bool cv = dt == FA_BF16;
+    if ((r = make_tile_map(&tq, cv ? q16 : q, cv ? FA_F16 : dt, N, s.BH, d, "q")) != FA_OK) return r;
     if ((r = make_tile_map(&tk, k, dt, N, BHkv, d, "k")) != FA_OK) return r;
     if ((r = make_tile_map(&tv, v, dt, N, BHkv, d, "v")) != FA_OK) return r;
-    if ((r = make_tile_map(&tdo, dout, dt, N, s.BH, d, "dout")) != FA_OK) return r;
+    if ((r = make_tile_map(&tdo, cv ? do16 : dout, cv ? FA_F16 : dt, N, s.BH, d, "dout")) != FA_OK)
+      return r;
   }
-  const size_t rows = padded_rows(B, H, N);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
   fa::BwdArgs a;
   a.dq = dq;
   a.dk = dk;
@@ -588,9 +608,17 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.lse = lse;
   a.lse_l2 = reinterpret_cast<float *>(ws);
   a.delta = reinterpret_cast<float *>(ws + up256(rows * 4));
+  a.q = q;
+  a.q16 = q16;
+  a.do16 = do16;
+  a.stats = stats;
   a.dq_acc = reinterpret_cast<float *>(ws + 2 * up256(rows * 4));
   a.kv_len = kv_len;
   a.block_mask = block_mask;
+  a.q = q;
+  a.q16 = q16;
+  a.do16 = do16;
+  a.stats = stats;
   a.H = H;
   a.N = N;
   a.nqt = s.nqt;
@@ -625,20 +653,43 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up once
-// per device (host code may not use the symbol itself as a pointer).
+// per device and context (host code may not use the symbol itself as a
+// pointer). The context is part of the key: after a device reset the
+// primary context is recreated, the module is loaded again and the array
+// may sit at a new address.
 fa_status noalloc_scratch(void **out) {
+  using CtxGetCurrent = CUresult (*)(CUcontext *);
+  static CtxGetCurrent ctx_get = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ctx_get = reinterpret_cast<CtxGetCurrent>(p);
+  });
   static std::mutex mu;
   static void *addr[64] = {};
+  static CUcontext ctx_of[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  if (ctx_get == nullptr) return fail(FA_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+  // no current context yet (first CUDA call of this thread): the lookup
+  // below makes the device's primary context current
+  CUcontext ctx = nullptr;
+  if (ctx_get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> g(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == nullptr || ctx_of[dev] != ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    if (ctx_get(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+      return fail(FA_ERR_CUDA, "cannot query the current CUDA context");
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return FA_OK;
@@ -788,8 +839,8 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   const int grid2 = static_cast<int>(s.BH * ((s.nqt + 1) / 2));
-  const bool launched = causal ? try_launch_fwd2<128, true, true, false, true>(tq, tk, tv, a, grid2, st, &r)
-                               : try_launch_fwd2<128, true, false, false, true>(tq, tk, tv, a, grid2, st, &r);
+  const bool launched = causal ? try_launch_fwd2<128, true, true, true>(tq, tk, tv, a, grid2, st, &r)
+                               : try_launch_fwd2<128, true, false, true>(tq, tk, tv, a, grid2, st, &r);
   if (!launched) return fail(FA_ERR_CUDA, "8-bit forward: kernel register count differs from its warpgroup split");
   if (r != FA_OK) return r;
   return ok();
@@ -952,6 +1003,8 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
                 "fa_bwd_noalloc: these sizes need %zu bytes of scratch, more than the %zu bytes "
                 "built into the library; use fa_bwd with a caller-owned workspace",
                 need, kNoAllocScratchBytes);
+  if (block_mask != nullptr && kv_len != nullptr)
+    return fail(FA_ERR_INVALID_ARG, "kv_len cannot be combined with a block mask");
   void *ws = nullptr;
   if ((r = noalloc_scratch(&ws)) != FA_OK) return r;
   const bool sparse = block_mask != nullptr;
@@ -971,8 +1024,26 @@ fa_status fa_get_device_error(void *stream) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(fa::g_fa_device_error, &zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_fail(e, "clear device error flag");
-    return fail(FA_ERR_TIMEOUT, "a kernel pipeline wait timed out (flag 0x%x)", v);
+    if (v & fa::kDevErrTimeout)
+      return fail(FA_ERR_TIMEOUT, "a kernel pipeline wait timed out (flag 0x%x)", v);
+    if (v & fa::kDevErrSmemAlign)
+      return fail(FA_ERR_CUDA, "a kernel's shared-memory base was not 1 KB aligned; it did no work (flag 0x%x)", v);
+    return fail(FA_ERR_RANGE, "a bf16 input of the backward exceeds 65504 in magnitude and was clamped (flag 0x%x)", v);
   }
+  return ok();
+}
+
+fa_status fa_set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long v = ns == 0 ? fa::kWaitLimitNs : ns;
+  const cudaError_t e = cudaMemcpyToSymbol(fa::g_fa_wait_limit_ns, &v, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "set the wait limit");
+  return ok();
+}
+
+fa_status fa_debug_starve_pipelines(int enable) {
+  const unsigned int v = enable ? 1u : 0u;
+  const cudaError_t e = cudaMemcpyToSymbol(fa::g_fa_starve_pipelines, &v, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "set the pipeline starvation switch");
   return ok();
 }
 
@@ -983,6 +1054,7 @@ const char *fa_status_str(fa_status s) {
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_RANGE: return "FA_ERR_RANGE";
   }
   return "FA_ERR_UNKNOWN";
 }

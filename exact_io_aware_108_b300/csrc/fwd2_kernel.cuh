@@ -19,8 +19,8 @@
 //   warps 8..11    softmax of tile B
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B after it.
 // P (16-bit pairs) is written into the first 64 columns of its own, already
-// read S buffer; with SPLIT the low part of P goes into the other 64. QK^T of
-// the next key tile into that buffer waits for the P V that reads it.
+// read S buffer. QK^T of the next key tile into that buffer waits for the
+// P V that reads it.
 //
 // Online softmax: softmax_row (softmax_row.cuh), the same arithmetic as
 // fwd_kernel.cuh.
@@ -75,11 +75,11 @@ struct Fwd2Cfg {
   static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kLaunchRegs * 384, "register split");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
+template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  static_assert(!FP8 || (BF16 && !SPLIT), "8-bit inputs give bf16 O, without residual");
+  static_assert(!FP8 || BF16, "8-bit inputs give bf16 O");
   using C = Fwd2Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw2[];
   const uint32_t raw = smem_u32(smem_raw2);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(384, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_max > 0) {
+    if (lane == 0 && n_max > 0 && !pipelines_starved()) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes * (has_b ? 2 : 1));
@@ -261,11 +261,6 @@ __global__ void __launch_bounds__(384, 1)
               for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
                 mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
                        (t > 0 || ks > 0) ? 1u : 0u);
-              if constexpr (SPLIT) {
-#pragma unroll
-                for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-                  mma_ts(ocol, pcol + 64 + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV, 1u);
-              }
             }
           }
           if (!ok) break;
@@ -335,7 +330,7 @@ __global__ void __launch_bounds__(384, 1)
       int limit = kvl - t * 128;
       if (CAUSAL && t == qt) limit = min(limit, row + 1);
       float m_new, alpha;
-      const float nm = softmax_max<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
       // rescale O_x first, so the P V of this tile can start right after the
       // first half of P. S_x(t) complete implies P_x V of tile t - 1 is done:
       // that product was finished before S_x(t) was issued.
@@ -362,10 +357,9 @@ __global__ void __launch_bounds__(384, 1)
       } else {
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t hi[16], lo[16];
-          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          uint32_t hi[16];
+          pack_p32<BF16>(s, c0, hi);
           tmem_st_32x32b_x16(scol + c0 / 2, hi);
-          if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
         }
       }
       tmem_wait_st();
@@ -381,10 +375,9 @@ __global__ void __launch_bounds__(384, 1)
       } else {
 #pragma unroll
         for (int c0 = 64; c0 < 128; c0 += 32) {
-          uint32_t hi[16], lo[16];
-          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          uint32_t hi[16];
+          pack_p32<BF16>(s, c0, hi);
           tmem_st_32x32b_x16(scol + c0 / 2, hi);
-          if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
         }
       }
       tmem_wait_st();

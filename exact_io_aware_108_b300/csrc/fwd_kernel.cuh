@@ -23,14 +23,10 @@
 // Online softmax in base 2: x = s * scale * log2(e); p = 2^(x - m);
 // l <- 2^(m_old - m) l + sum p; O <- 2^(m_old - m) O + P V
 // (softmax decomposition and merger, section "The Math Behind Flash
-// Attention"; the per-row update is softmax_row in softmax_row.cuh). Without
-// SPLIT m is the exact running row max, so the largest probability of a row
-// is exactly 1 when it is rounded to 16 bits for the P V product, and O is
-// rescaled in TMEM whenever any row of the warp sees a new max. (A lagging max
-// rounds the dominant probability too: for sharp bf16 softmax that doubled
-// the error of O and of D = rowsum(dO * O).) With SPLIT the P_lo product
-// recovers that rounding, so m may lag the max by up to a factor 2^8 and most
-// tiles need no rescale.
+// Attention"; the per-row update is softmax_row in softmax_row.cuh). m is the
+// exact running row max, so the largest probability of a row is exactly 1
+// when it is rounded to 16 bits for the P V product, and O is rescaled in
+// TMEM whenever any row of the warp sees a new max.
 #pragma once
 #include "common.cuh"
 #include "softmax_row.cuh"
@@ -98,14 +94,7 @@ struct FwdCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// SPLIT (the caller asked for O's rounding residual, i.e. for an O accurate
-// enough to form D = rowsum(dO * O) in the backward): each probability p is
-// sent to the tensor core as p_hi = bf16/f16(p) and p_lo = bf16/f16(p - p_hi),
-// and O += P_hi V + P_lo V, so O carries the rounding of P only to second
-// order. P_lo of tile t is written into the upper half of its own S buffer
-// (already read), and the MMA thread waits for P V of tile t to finish before
-// QK^T of tile t + 2 overwrites that buffer.
-template <int D, bool BF16, bool CAUSAL, bool SPARSE, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -183,7 +172,7 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_tiles > 0 && !pipelines_starved()) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes);
@@ -244,13 +233,6 @@ __global__ void __launch_bounds__(256, 1)
               const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
               mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
             }
-            if constexpr (SPLIT) {
-              const uint32_t lcol = tmem + (pb ? C::kColS1 : C::kColS0) + 64;
-#pragma unroll
-              for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-                mma_ts(tmem + C::kColO, lcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024),
-                       kIdPV, 1u);
-            }
           }
         }
         mma_commit(bar(C::kBVE + st));
@@ -262,8 +244,6 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t ph = (t / C::kStages) & 1;
         const int sb = t & 1;
         if (!mbar_wait(bar(C::kBKF + st), ph, abort_flag)) { ok = false; break; }
-        // SPLIT: P_lo of tile t - 2 lives in this S buffer until its P V is done
-        if (SPLIT && t >= 2 && !mbar_wait(bar(C::kBOR), (t - 2) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
         const uint32_t scol = tmem + (sb ? C::kColS1 : C::kColS0);
@@ -331,17 +311,15 @@ __global__ void __launch_bounds__(256, 1)
       int limit = kvl - kt * 128;
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
       float m_new, alpha;
-      const float rs = softmax_row<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      const float rs = softmax_row(s, limit, sl2, m, m_new, alpha);
       l = l * alpha + rs;
       {
         const uint32_t pcol = tmem + lane_addr + (sb ? C::kColP1 : C::kColP0);
-        const uint32_t lcol = tmem + lane_addr + (sb ? C::kColS1 : C::kColS0) + 64;
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t hi[16], lo[16];
-          pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+          uint32_t hi[16];
+          pack_p32<BF16>(s, c0, hi);
           tmem_st_32x32b_x16(pcol + c0 / 2, hi);
-          if constexpr (SPLIT) tmem_st_32x32b_x16(lcol + c0 / 2, lo);
         }
       }
       if (t > 0) {

@@ -7,8 +7,8 @@
 // start-up (barrier set-up, TMEM allocation, first Q/K/V latency) and its
 // epilogue are a large part of its life; a second resident CTA runs its
 // tiles meanwhile. 256 threads launched with 128 registers each, 256 TMEM
-// columns (S, into which P -- and with SPLIT its low part in columns
-// 64..127 -- is written once S is read, then O), one K and one V stage.
+// columns (S, into which P is written once S is read, then O), one K and
+// one V stage.
 //
 // Roles (setmaxnreg moves registers from warpgroup 1 to warpgroup 0):
 //   warps 0..3     softmax, one query row per thread (TMEM lanes 0..127)
@@ -17,8 +17,8 @@
 //   warps 6, 7     idle
 // Per key tile t the MMA thread issues S = Q K_t^T once P(t-1) V(t-1) is
 // done (S holds P), then O += P(t) V(t) once P(t) and V(t) are in place.
-// The arithmetic per row and the P V product order (two 64-key halves, high
-// then low part of each) are those of the two-tile kernel.
+// The arithmetic per row and the P V product order (two 64-key halves) are
+// those of the two-tile kernel.
 #pragma once
 #include "common.cuh"
 #include "fwd_kernel.cuh"
@@ -58,7 +58,7 @@ struct SmallCfg {
   static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory for two CTAs per SM");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(256, 2)
     fwd_small_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256, 2)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_tiles > 0 && !pipelines_starved()) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBQ), C::kTileBytes);
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256, 2)
         mma_commit(bar(C::kBKE));
         if (!mbar_wait(bar(C::kBVF), ph, abort_flag)) { ok = false; break; }
         const uint32_t vbase = sb + C::kVOff;
-        // O += P(t) V(t) in two halves of 64 keys, high then low part of each
+        // O += P(t) V(t) in two halves of 64 keys
         for (int h = 0; h < 2; ++h) {
           if (!mbar_wait(bar(C::kBPF + h), ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -177,12 +177,6 @@ __global__ void __launch_bounds__(256, 2)
             // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
             mma_ts(tmem + C::kColO, tmem + C::kColS + k * 8, sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdPV,
                    (t > 0 || k > 0) ? 1u : 0u);
-          if constexpr (SPLIT) {
-#pragma unroll
-            for (int k = 4 * h; k < 4 * h + 4; ++k)
-              mma_ts(tmem + C::kColO, tmem + C::kColS + 64 + k * 8, sdesc_sw128(vbase + k * 2048, 16384, 1024),
-                     kIdPV, 1u);
-          }
         }
         if (!ok) break;
         mma_commit(bar(C::kBVE));
@@ -247,7 +241,7 @@ __global__ void __launch_bounds__(256, 2)
       int limit = kvl - t * 128;
       if (CAUSAL && t == qt) limit = min(limit, row + 1);
       float m_new, alpha;
-      const float nm = softmax_max<SPLIT>(s, limit, sl2, m, m_new, alpha);
+      const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
       // S(t) complete implies P(t-1) V(t-1) is done (S(t) waited for it): O
       // holds every earlier tile and can be rescaled
       if (t > 0 && __any_sync(0xffffffffu, m_new != m)) {
@@ -265,10 +259,9 @@ __global__ void __launch_bounds__(256, 2)
       softmax_exp<0, 64>(s, sl2, nm, acc);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t hi[16], lo[16];
-        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+        uint32_t hi[16];
+        pack_p32<BF16>(s, c0, hi);
         tmem_st_32x32b_x16(scol + c0 / 2, hi);
-        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -276,10 +269,9 @@ __global__ void __launch_bounds__(256, 2)
       softmax_exp<64, 128>(s, sl2, nm, acc);
 #pragma unroll
       for (int c0 = 64; c0 < 128; c0 += 32) {
-        uint32_t hi[16], lo[16];
-        pack_p32<BF16, SPLIT>(s, c0, hi, lo);
+        uint32_t hi[16];
+        pack_p32<BF16>(s, c0, hi);
         tmem_st_32x32b_x16(scol + c0 / 2, hi);
-        if constexpr (SPLIT) tmem_st_32x32b_x16(scol + 64 + c0 / 2, lo);
       }
       tmem_wait_st();
       tc_fence_before();

@@ -6,9 +6,11 @@
 // In base 2 ("Flash Attention: revolutionizing transformer efficiency",
 // section "The Math Behind Flash Attention": softmax decomposition and
 // merger): x_c = s_c * scale * log2(e); the running max m moves to
-// max(m, max_c x_c) (LAZY: only when that exceeds m by more than 8, i.e. a
-// factor 256); p_c = 2^(x_c - m_new); alpha = 2^(m_old - m_new); the caller
-// updates l <- alpha l + sum_c p_c and O <- alpha O + P V.
+// max(m, max_c x_c); p_c = 2^(x_c - m_new); alpha = 2^(m_old - m_new); the
+// caller updates l <- alpha l + sum_c p_c and O <- alpha O + P V. The max is
+// exact, so the largest probability of a row is exactly 1 when it is rounded
+// to 16 bits for the P V product (a lagging max rounds the dominant
+// probability too: for sharp bf16 softmax that doubled the error of O).
 #pragma once
 #include "ptx.cuh"
 
@@ -17,7 +19,6 @@ namespace fa {
 // Masks entries c >= limit of s (the 128 raw scores of this row) and
 // moves the running max: returns -m_use, the offset of the exponent, and
 // sets m_new and alpha = 2^(m - m_new).
-template <bool LAZY>
 __device__ __forceinline__ float softmax_max(float (&s)[128], int limit, float sl2, float m,
                                              float &m_new, float &alpha) {
   if (limit < 128) {
@@ -37,7 +38,7 @@ __device__ __forceinline__ float softmax_max(float (&s)[128], int limit, float s
   mx0 = fmax3(mx0, s[124], s[125]);
   mx1 = fmax3(mx1, s[126], s[127]);
   const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-  m_new = LAZY ? ((mxs > m + 8.0f) ? mxs : m) : fmaxf(m, mxs);
+  m_new = fmaxf(m, mxs);
   const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
   alpha = ex2_approx(m - m_use);
   return -m_use;
@@ -66,29 +67,19 @@ __device__ __forceinline__ float softmax_sum(const float (&acc)[4]) {
 
 // The whole row update: on return s holds p (fp32); returns the tile's sum
 // of p. Same arithmetic as softmax_max + softmax_exp<0, 128> + softmax_sum.
-template <bool LAZY>
 __device__ __forceinline__ float softmax_row(float (&s)[128], int limit, float sl2, float m,
                                              float &m_new, float &alpha) {
-  const float nm = softmax_max<LAZY>(s, limit, sl2, m, m_new, alpha);
+  const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   softmax_exp<0, 128>(s, sl2, nm, acc);
   return softmax_sum(acc);
 }
 
-// Packs p (fp32) of columns c0 .. c0+31 into 16 16-bit pairs (hi) and, for
-// the split product, the rounding remainders (lo).
-template <bool BF16, bool SPLIT>
-__device__ __forceinline__ void pack_p32(const float (&s)[128], int c0, uint32_t (&hi)[16],
-                                         uint32_t (&lo)[16]) {
+// Packs p (fp32) of columns c0 .. c0+31 into 16 16-bit pairs.
+template <bool BF16>
+__device__ __forceinline__ void pack_p32(const float (&s)[128], int c0, uint32_t (&hi)[16]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    hi[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
-    if constexpr (SPLIT) {
-      float r0, r1;
-      fsub2(r0, r1, s[c0 + 2 * i], s[c0 + 2 * i + 1], unpack_lo<BF16>(hi[i]), unpack_hi<BF16>(hi[i]));
-      lo[i] = pack2<BF16>(r0, r1);
-    }
-  }
+  for (int i = 0; i < 16; ++i) hi[i] = pack2<BF16>(s[c0 + 2 * i], s[c0 + 2 * i + 1]);
 }
 
 // O row chunk (32 fp32 values) *= alpha.

@@ -84,7 +84,8 @@ WORKLOADS = {
         "blocksparse_b2_h8_n16384_d64_f16", 2, 8, 16384, 64, "f16", block_sparse_p=0.2),
     # grouped-query attention (32 query heads sharing 8 key/value heads)
     "gqa_b4_h32_hkv8_n4096_d128_bf16_causal": Workload(
-        "gqa_b4_h32_hkv8_n4096_d128_bf16_causal", 4, 32, 4096, 128, "bf16", causal=True, hkv=8),
+        "gqa_b4_h32_hkv8_n4096_d128_bf16_causal", 4, 32, 4096, 128, "bf16", causal=True, hkv=8,
+        qk_mult=2.0),
     # the N = 8192 long-context point with 8-bit q, k, v
     "fp8_b4_h16_n8192_d128_e4m3_causal": Workload(
         "fp8_b4_h16_n8192_d128_e4m3_causal", 4, 16, 8192, 128, "e4m3", causal=True, backward=False),

@@ -41,14 +41,22 @@
  *           call is asynchronous on that stream and never synchronises, except
  *           fa_get_device_error.
  * Numerics  inputs are read as fp16/bf16; every product is accumulated in fp32;
- *           the softmax runs in fp32 with exp2; probabilities are rounded to
- *           the input type before the P V product.
+ *           the softmax runs in fp32 with exp2. The forward rounds the
+ *           probabilities to the input type before the P V product. The
+ *           backward runs all five of its products on fp16 operands whatever
+ *           the input type (P and dS rounded to fp16, 11 significant bits;
+ *           bf16 Q, K, V converted to fp16, which is exact for
+ *           2^-17 <= |x| <= 65504; bf16 dO converted after scaling by a
+ *           power of two chosen from max |dO|), so sharp softmax does not
+ *           lose its gradients to bf16's 8-bit significand.
  * Errors    argument checks run on the host before any launch and return
  *           FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED without touching memory.
  *           A failed launch returns FA_ERR_CUDA. A pipeline wait inside a
  *           kernel that exceeds its time limit (about two seconds; it cannot
  *           happen in a correct build) makes the kernel stop early and sets a
  *           device flag that fa_get_device_error reports as FA_ERR_TIMEOUT.
+ *           A bf16 q, k or v value beyond +-65504 given to the backward is
+ *           clamped and reported the same way as FA_ERR_RANGE.
  *           fa_last_error_message() gives the detail of the last failure on
  *           the calling thread.
  */
@@ -67,7 +75,8 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer   */
     FA_ERR_UNSUPPORTED = 2,  /* valid but not built: d not in {64, 128}     */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed           */
-    FA_ERR_TIMEOUT = 4       /* a kernel pipeline wait ran out (device flag) */
+    FA_ERR_TIMEOUT = 4,      /* a kernel pipeline wait ran out (device flag) */
+    FA_ERR_RANGE = 5         /* a bf16 input of the backward beyond +-65504 (device flag) */
 } fa_status;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -256,8 +265,10 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int causal, int
  * Bytes of device workspace fa_bwd / fa_bwd_blocksparse need for these
  * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
  * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ
- * accumulator [R, d], each rounded up to 256 bytes. Returns 0 for invalid
- * sizes.
+ * accumulator [R, d], each rounded up to 256 bytes; 256 bytes of statistics
+ * (max |dO|, max |D|); then room for fp16 copies of Q and of the scaled dO
+ * ([B, H, N, d] each, rounded up to 256 bytes; used for bf16 inputs only).
+ * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -309,10 +320,14 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
  * time them separately (fa_bwd == prepare; main; finish on one stream, same
  * workspace). Arguments mean what they mean for fa_bwd / fa_bwd_blocksparse.
  *   fa_bwd_prepare  D = rowsum(dO * (O + o_res)) and LSE * log2(e) into the
- *                   workspace; zeroes the workspace's fp32 dQ accumulator.
- *   fa_bwd_main     one CTA per 128-key tile: dK and dV (written directly),
- *                   dQ partials added into the accumulator. block_mask NULL
- *                   means dense/causal (causal applies only then).
+ *                   workspace; zeroes the workspace's fp32 dQ accumulator;
+ *                   records max |dO| and max |D|.
+ *   fa_bwd_main     (bf16 inputs: first the fp16 copies of Q and the scaled
+ *                   dO into the workspace) one CTA per 128-key tile: dK and
+ *                   dV (written directly), dQ partials added into the
+ *                   accumulator. block_mask NULL means dense/causal (causal
+ *                   applies only then); kv_len must be NULL when block_mask
+ *                   is given (FA_ERR_INVALID_ARG otherwise).
  *   fa_bwd_finish   dQ accumulator -> dq (fp16/bf16).
  */
 fa_status fa_bwd_prepare(const void *o, const void *o_res, const float *lse, const void *dout,
@@ -336,17 +351,19 @@ fa_status fa_bwd_finish(void *dq, int B, int H, int N, int d, fa_dtype dtype, vo
  * scratch array built into the library instead; everything else (inputs and
  * outputs) is still passed in, exactly as for fa_bwd / fa_bwd_blocksparse.
  *   block_mask  NULL: dense or causal (as fa_bwd); non-NULL: block-sparse
- *               (as fa_bwd_blocksparse; causal is ignored).
+ *               (as fa_bwd_blocksparse; causal is ignored, and kv_len must
+ *               be NULL: FA_ERR_INVALID_ARG otherwise).
  * Limits and behaviour:
  *   - the scratch holds fa_bwd_noalloc_max_workspace() bytes (32 MiB); sizes
  *     whose fa_bwd_workspace_size exceeds it are rejected with
  *     FA_ERR_INVALID_ARG before anything runs (for d = 128 that is about
- *     64K query rows: B * H * ceil(N / 128) * 128 <= 64527);
+ *     32K query rows: B * H * N <= 32512 when N is a multiple of 128);
  *   - the array is part of the library's device image: every GPU that loads
  *     the library holds it until the process exits;
  *   - the first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture;
+ *     per device and CUDA context, with that device current; a context that
+ *     was reset and recreated is looked up again); make that first call
+ *     before any stream capture;
  *   - all calls share the one array and it keeps the last call's contents;
  *     each call rewrites every part it reads (the dQ accumulator is zeroed
  *     by the call itself), but two calls that overlap on the GPU (different
@@ -364,11 +381,36 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
 size_t fa_bwd_noalloc_max_workspace(void);
 
 /*
- * Synchronises `stream`, then reads and clears the device error flag set by
- * a kernel whose pipeline wait timed out. Returns FA_OK, FA_ERR_TIMEOUT or
- * FA_ERR_CUDA (when the synchronisation itself failed).
+ * Synchronises `stream`, then reads and clears the device error word. Returns
+ * FA_OK; FA_ERR_TIMEOUT when a kernel's pipeline wait timed out;
+ * FA_ERR_CUDA when a kernel found its shared memory misaligned (it did no
+ * work) or the synchronisation itself failed; FA_ERR_RANGE when the backward
+ * clamped a bf16 input beyond +-65504. Several conditions: the first in
+ * that order.
  */
 fa_status fa_get_device_error(void *stream);
+
+/*
+ * Time limit of the kernels' pipeline waits on the current device, in
+ * nanoseconds (0 restores the default of 2 s). A wait that runs out stops
+ * its kernel early and sets the flag fa_get_device_error reports as
+ * FA_ERR_TIMEOUT; a lower limit detects a stuck pipeline sooner. Waits for
+ * copies already in flight after such a stop always allow the default, so
+ * those copies land before the kernel exits. Synchronous; do not call while
+ * kernels of this library run.
+ */
+fa_status fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Test switch of the failure path (no counterpart in the pages). enable != 0
+ * makes the load-issuing thread of every attention kernel on the current
+ * device issue nothing, so each kernel's first pipeline wait can only run
+ * out: the kernels then stop early, write zero outputs and set the
+ * FA_ERR_TIMEOUT flag, which exercises the time limit, the abort of the
+ * other roles and fa_get_device_error without any fault. Pair it with a low
+ * fa_set_wait_limit_ns. enable == 0 restores normal operation. Synchronous.
+ */
+fa_status fa_debug_starve_pipelines(int enable);
 
 /* Static string naming a status code. */
 const char *fa_status_str(fa_status status);

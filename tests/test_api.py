@@ -31,6 +31,7 @@ def test_library_exports_every_declared_symbol():
 def test_status_strings_and_version():
     assert fa.fa_status_str(0) == "FA_OK"
     assert fa.fa_status_str(4) == "FA_ERR_TIMEOUT"
+    assert fa.fa_status_str(5) == "FA_ERR_RANGE"
     assert re.match(r"^\d+\.\d+\.\d+$", fa.fa_version())
 
 
@@ -38,7 +39,9 @@ def test_workspace_size():
     def up(x):
         return (x + 255) // 256 * 256
     rows = 2 * 3 * 384  # query rows padded to whole 128-row tiles
-    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * up(rows * 4) + up(rows * 64 * 4)
+    elems = 2 * 3 * 300 * 64  # fp16 copies of Q and of the scaled dO (bf16 inputs)
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == (2 * up(rows * 4) + up(rows * 64 * 4) + 256
+                                                      + 2 * up(elems * 2))
     assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
@@ -84,6 +87,23 @@ def test_bwd_rejects_bad_arguments():
     # block-sparse without a mask
     st = lib.fa_bwd_blocksparse(*args, 1, 1, 128, 64, c, 0, None, None, FAKE, 1 << 30, None)
     assert st == 1
+
+
+def test_bwd_rejects_key_padding_with_a_block_mask():
+    """No forward computes block-sparse attention with key padding, so the
+    backward entry points that take both refuse the combination."""
+    lib = fa.load_library()
+    c = ctypes.c_float(0.125)
+    st = lib.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, c, 0, 0, FAKE, FAKE,
+                         FAKE, 1 << 30, None)
+    assert st == 1 and "kv_len" in fa.fa_last_error_message()
+    st = lib.fa_bwd_noalloc(*([FAKE] * 9), 1, 1, 256, 64, c, 0, 0, FAKE, FAKE, None, None)
+    assert st == 1 and "kv_len" in fa.fa_last_error_message()
+    # either one alone passes the argument checks of fa_bwd_main up to the
+    # workspace test (too small here, so nothing is launched)
+    st = lib.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, c, 0, 0, FAKE, None,
+                         FAKE, 16, None)
+    assert st == 1 and "workspace" in fa.fa_last_error_message()
 
 
 def test_gqa_rejects_bad_head_counts():

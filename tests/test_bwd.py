@@ -7,6 +7,7 @@ import torch
 
 from exact_io_aware_108_b300 import inputs
 from oracle import ref
+from tests.sampled import check_bwd_every_head
 from tests.tolerance import TOL_GRAD, check
 
 pytestmark = pytest.mark.gpu
@@ -144,3 +145,16 @@ def test_bwd_full_size_whole_heads(name):
         check(f"dQ[{b},{h}]", dq[b, h], g[0][0, 0], TOL_GRAD, dt)
         check(f"dK[{b},{h}]", dk[b, h], g[1][0, 0], TOL_GRAD, dt)
         check(f"dV[{b},{h}]", dv[b, h], g[2][0, 0], TOL_GRAD, dt)
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_bwd_full_size_every_head_sampled(name):
+    """Full-size workload, same launches as the benchmark; dQ at sampled
+    query rows and dK, dV at sampled key rows of EVERY head (tile edges and
+    seeded random rows) against the oracle."""
+    w = inputs.WORKLOADS[name]
+    t = inputs.make_workload(w, with_dout=True)
+    dq, dk, dv = run_bwd(t, w.scale, w.causal, t.get("kv_len"), t.get("block_mask"))
+    worst = check_bwd_every_head(t, w, dq, dk, dv)
+    print(f"\n{name}: max |d grad| over sampled rows of every head: "
+          + ", ".join(f"{k} {v:.4g}" for k, v in worst.items()))

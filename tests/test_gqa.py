@@ -11,6 +11,7 @@ import torch
 
 from exact_io_aware_108_b300 import inputs
 from oracle import ref
+from tests.sampled import check_bwd_every_head
 from tests.tolerance import TOL_GRAD, TOL_LSE, TOL_O, check, half_ulp
 
 pytestmark = pytest.mark.gpu
@@ -70,6 +71,14 @@ def test_gqa_with_key_padding():
     _compare(t, 4, 2, 1.0 / math.sqrt(128), False, t["kv_len"])
 
 
+def test_gqa_sharp_matches_oracle():
+    """Sharp softmax (Q, K x2, logit std 4) with grouped heads and key padding:
+    the group sums of dK and dV collect the rounding of four heads."""
+    t = inputs.make_qkv(2, 8, 640, 128, "bf16", seed=35, qk_mult=2.0, hkv=2,
+                        kv_len_range=(300, 640))
+    _compare(t, 8, 2, 1.0 / math.sqrt(128), True, t["kv_len"])
+
+
 def test_gqa_sharp_equals_plain_path_on_repeated_kv():
     """Sharp softmax (Q, K x2) with key padding: the grouped path computes
     exactly what the plain path computes on K and V repeated per group: O
@@ -123,15 +132,16 @@ def test_gqa_with_hkv_equal_h_is_the_plain_path():
 
 
 def test_gqa_full_size_whole_heads():
-    """The benchmark-sized grouped workload: every dK and dV element of one
-    key/value head (the sum over its four query heads) and every O, LSE and
-    dQ element of one of those query heads, against the oracle."""
+    """The benchmark-sized grouped workload (sharp softmax: Q and K x 2):
+    every dK and dV element of two key/value heads (the sums over their four
+    query heads) and every O, LSE and dQ element of one of those query heads,
+    against the oracle."""
     w = inputs.WORKLOADS["gqa_b4_h32_hkv8_n4096_d128_bf16_causal"]
     t = inputs.make_workload(w, with_dout=True)
     o, lse, dq, dk, dv = _run(t, w.scale, w.causal)
     g = w.H // w.hkv
     dt = t["q"].dtype
-    for b, hkv in ((w.B - 1, 1),):
+    for b, hkv in ((w.B - 1, 1), (0, w.hkv - 1)):
         hs = slice(hkv * g, (hkv + 1) * g)
         kr = _repeat(t["k"][b:b + 1, hkv:hkv + 1], g)
         vr = _repeat(t["v"][b:b + 1, hkv:hkv + 1], g)
@@ -145,3 +155,14 @@ def test_gqa_full_size_whole_heads():
         check(f"dQ[{b},{h0}]", dq[b, h0], grads[0][0, 0], TOL_GRAD, dt)
         check(f"dK[{b},{hkv}]", dk[b, hkv], np.asarray(grads[1])[0].sum(axis=0), TOL_GRAD, dt)
         check(f"dV[{b},{hkv}]", dv[b, hkv], np.asarray(grads[2])[0].sum(axis=0), TOL_GRAD, dt)
+
+
+def test_gqa_full_size_every_head_sampled():
+    """The same workload: dQ at sampled rows of every query head, dK and dV
+    (group sums) at sampled rows of every key/value head, against the oracle."""
+    w = inputs.WORKLOADS["gqa_b4_h32_hkv8_n4096_d128_bf16_causal"]
+    t = inputs.make_workload(w, with_dout=True)
+    _, _, dq, dk, dv = _run(t, w.scale, w.causal)
+    worst = check_bwd_every_head(t, w, dq, dk, dv, seed=1)
+    print("\ngqa sharp: max |d grad| over sampled rows of every head: "
+          + ", ".join(f"{k} {v:.4g}" for k, v in worst.items()))

@@ -55,3 +55,29 @@ def check(name, got, ref, tol, dtype, report=None):
             f"{name}: {int(over.sum())}/{over.size} elements out of tolerance; worst at {tuple(idx)}: "
             f"gpu {g[tuple(idx)]!r} ref {r[tuple(idx)]!r} (tol {tol} + ulp/2)")
     return worst, float(np.max(np.abs(r[fin]), initial=0.0))
+
+
+# Unit roundoff (half an ulp at 1) of the 16-bit types: round to nearest
+# even moves a normal value by at most this fraction of itself.
+UNIT_ROUNDOFF = {torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+
+
+def check_residual(name, o, o_res, o_ref, o_abs_ref, dtype, slack=2e-4):
+    """O + o_res is the fp32 result of the P V product before its rounding to
+    16 bits. The forward rounds each probability p (<= 1) to the input type
+    before that product, which moves p by at most u p (u the unit roundoff;
+    fp16 values below 2^-14 by at most 2^-25), so every element obeys
+    |O + o_res - O_exact| <= u * (attention applied to |V|) + slack, the slack
+    covering fp32 accumulation, ex2.approx and the rounding of o_res itself.
+    o_abs_ref is the oracle's attention on |V| for the same scores."""
+    got = to_np(o) + to_np(o_res)
+    r = np.asarray(o_ref, dtype=np.float64)
+    bound = UNIT_ROUNDOFF[dtype] * np.asarray(o_abs_ref, dtype=np.float64) + slack
+    diff = np.abs(got - r)
+    over = diff > bound
+    if np.any(over):
+        idx = np.unravel_index(np.argmax(diff - bound), diff.shape)
+        raise AssertionError(f"{name}: {int(over.sum())}/{over.size} elements of O + o_res beyond "
+                             f"u |O|_abs + {slack}; worst at {idx}: {got[idx]!r} vs {r[idx]!r} "
+                             f"(bound {bound[idx]!r})")
+    return float(diff.max(initial=0.0))
