@@ -78,6 +78,7 @@
 // the dP^T columns for d = 128 and has its own 64 columns for d = 64.
 #pragma once
 #include "common.cuh"
+#include "schedule.cuh"
 
 namespace fa {
 
@@ -104,9 +105,7 @@ struct BwdArgs {
   int kv_group;  // query heads per key/value head
   float scale, scale_log2;
   // [B*H] index of query head g of the group that reads key/value head bkv
-  __device__ __forceinline__ int q_head(int bkv, int g) const {
-    return (bkv / Hkv) * H + (bkv % Hkv) * kv_group + g;
-  }
+  __device__ __forceinline__ int q_head(int bkv, int g) const { return q_head_of(bkv, g, H, Hkv); }
 };
 
 // 1-D bulk copy global -> shared, completion as transaction bytes on bar.
@@ -292,7 +291,9 @@ struct BwdCfg {
   static constexpr int kBarOff = kDeltaOff + 1024;
   static constexpr int kBKV = 0, kBQF = 1, kBQE = 3, kBSF = 5, kBDPF = 6, kBPR = 7 /* x2 */,
                        kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13, kBDSF = 14,
-                       kBCV = 15 /* K, V ready in fp16, 384 arrivals */, kNumBars = 16;
+                       kBCK = 15 /* K ready in fp16, 384 arrivals */,
+                       kBCV = 16 /* V ready in fp16, max |V_j| slots written, 384 arrivals */,
+                       kNumBars = 17;
   // d = 128: the dQ partial is computed transposed (dQ^T = K^T dS^T, TMEM
   // lane = head-dim channel, column = query) so one warp's reduction into
   // the fp32 accumulator covers 32 consecutive channels of a row: a whole
@@ -345,15 +346,10 @@ __global__ void __launch_bounds__(512, 1)
   // so the heaviest CTAs of the group (causal: low key tiles see the most
   // query tiles) start first, while the heads that run concurrently stay
   // few enough for their Q and dO to stay in L2.
-  int bkv, kt;  // key/value head ([B*Hkv] index) and key tile of this CTA
-  {
-    const int BH = static_cast<int>(gridDim.x) / a.nkt;
-    const int grp = static_cast<int>(blockIdx.x) / (a.hgroup * a.nkt);
-    const int rem = static_cast<int>(blockIdx.x) - grp * a.hgroup * a.nkt;
-    const int nh = min(a.hgroup, BH - grp * a.hgroup);
-    kt = rem / nh;
-    bkv = grp * a.hgroup + rem % nh;
-  }
+  // key/value head ([B*Hkv] index) and key tile of this CTA
+  const WorkItem item =
+      grouped_item(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x) / a.nkt, a.nkt, a.hgroup, false);
+  const int bkv = item.bh, kt = item.tile;
   const int b = bkv / a.Hkv;
   int kvl = a.N;
   if (a.kv_len != nullptr) {
@@ -398,6 +394,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(C::kBDQE), 128);
     mbar_init(bar(C::kBFIN), 1);
     mbar_init(bar(C::kBDSF), 1);
+    mbar_init(bar(C::kBCK), 384);
     mbar_init(bar(C::kBCV), 384);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -472,7 +469,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(bar(C::kBSF));
       };
-      bool ok = mbar_wait(bar(C::kBCV), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
+      bool ok = mbar_wait(bar(C::kBCK), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -485,6 +482,8 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t sdO = sb + C::kdOOff + st * C::kTileBytes;
         // d = 128: the dP^T columns hold the previous dQ partial until read out
         if (C::kDqT && u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
+        // the first dP^T needs V in fp16
+        if (u == 0 && !mbar_wait(bar(C::kBCV), 0, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
@@ -561,34 +560,40 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // ---- prologue of warpgroups 1-3: K_j, V_j -> fp16 in place (bf16
-    // inputs), max |V_j| per warp into shared memory
+    // ---- prologue of warpgroups 1-3: K_j -> fp16 in place (bf16 inputs),
+    // then V_j and its max |V_j| per warp into shared memory. The first S^T
+    // needs only K; the first dP^T and the dS exponent wait for V.
     float *slots = reinterpret_cast<float *>(misc + 4);
     if (n_iter > 0) {
+      constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
       float amax_v = 0.f, amax_k = 0.f;
-      if (mbar_wait_warp(bar(C::kBKV), 0, abort_flag)) {
-        constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
-        uint4 *kv = reinterpret_cast<uint4 *>(smem + C::kKOff);  // K then V (adjacent)
-        static_assert(C::kVOff == C::kKOff + C::kTileBytes, "K and V tiles are adjacent");
-        for (int c = tid - 128; c < 2 * kChunks; c += 384) {
-          const uint4 w = kv[c];
-          if constexpr (BF16) {
-            float m = 0.f;
-            kv[c] = bf16x8_to_f16x8(w, m);
-            if (c < kChunks) amax_k = fmaxf(amax_k, m); else amax_v = fmaxf(amax_v, m);
-          } else if (c >= kChunks) {
-            amax_v = fmaxf(amax_v, amax16x8<false>(w));
-          }
+      const bool landed = mbar_wait_warp(bar(C::kBKV), 0, abort_flag);
+      if (BF16 && landed) {
+        uint4 *kt16 = reinterpret_cast<uint4 *>(smem + C::kKOff);
+        for (int c = tid - 128; c < kChunks; c += 384) kt16[c] = bf16x8_to_f16x8(kt16[c], amax_k);
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kBCK));
+      if (landed) {
+        uint4 *vt16 = reinterpret_cast<uint4 *>(smem + C::kVOff);
+        for (int c = tid - 128; c < kChunks; c += 384) {
+          if constexpr (BF16)
+            vt16[c] = bf16x8_to_f16x8(vt16[c], amax_v);
+          else
+            amax_v = fmaxf(amax_v, amax16x8<false>(vt16[c]));
         }
         if (BF16 && fmaxf(amax_k, amax_v) > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
         if (BF16) fence_proxy_async_smem();
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBCV));
 #pragma unroll
       for (int s2 = 16; s2 > 0; s2 >>= 1) amax_v = fmaxf(amax_v, __shfl_xor_sync(0xffffffffu, amax_v, s2));
       if (lane == 0) slots[warp - 4] = amax_v;
-      named_bar_sync(2, 384);
+      __syncwarp();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBCV));
+      // every thread of warpgroups 1-3 reads the slots (the dS exponent) next
+      mbar_wait_warp(bar(C::kBCV), 0, abort_flag);
     }
     // e_s: |dS| <= |dP| + |D| <= d max|dO| max|V_j| + max|D| (clamped values
     // are at most 65504, so the bound stays finite for finite inputs); dS is

@@ -224,10 +224,10 @@ int sm_count();
 // two-tile kernel it relies on setmaxnreg, so it runs only when built with
 // exactly the register count its split assumes (checked once per kernel and
 // device); returns false (nothing launched) otherwise.
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE = false>
 bool try_launch_fwd_small(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const fa::FwdArgs &a, int grid, cudaStream_t st, fa_status *r) {
-  auto kern = fa::fwd_small_kernel<D, BF16, CAUSAL>;
+  auto kern = fa::fwd_small_kernel<D, BF16, CAUSAL, SPARSE>;
   static std::mutex mu;
   static int usable[64] = {};  // 0 unknown, 1 yes, -1 no
   int dev = 0;
@@ -282,17 +282,22 @@ fa_status launch_merge(const fa::FwdArgs &a, long long rows, int d, cudaStream_t
 template <int D, bool BF16>
 fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
-  if (sparse) return launch_fwd_t<D, BF16, false, true>(tq, tk, tv, a, grid, st);
+  fa_status r = FA_OK;
+  if (sparse) {
+    // block-sparse: one query tile per CTA, two CTAs per SM, each walking
+    // its own row's kept key tiles
+    if (try_launch_fwd_small<D, BF16, false, true>(tq, tk, tv, a, grid, st, &r)) return r;
+    return launch_fwd_t<D, BF16, false, true>(tq, tk, tv, a, grid, st);
+  }
   if (a.num_splits > 1) {
     // split-KV: single-tile kernel over (query tile, split), then the merge
-    const fa_status r = causal ? launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st)
-                               : launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
+    r = causal ? launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st)
+               : launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
     if (r != FA_OK) return r;
     return launch_merge<BF16>(a, static_cast<long long>(grid / a.nqt) * a.N, D, st);
   }
   // short sequences: one query tile per CTA, two CTAs per SM (the start-up
   // and epilogue of one CTA overlap the other's tiles)
-  fa_status r = FA_OK;
   if ((a.nqt <= kSmallMaxTiles || (grid / a.nqt) * ((a.nqt + 1) / 2) < sm_count()) &&
       (causal ? try_launch_fwd_small<D, BF16, true>(tq, tk, tv, a, grid, st, &r)
               : try_launch_fwd_small<D, BF16, false>(tq, tk, tv, a, grid, st, &r)))
@@ -511,11 +516,9 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     fa::bwd_pre_kernel<D, BF16><<<static_cast<int>(pre_blocks), 256, 0, st>>>(a, rows_pad);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "bwd prepare launch");
-  }
-  if (phases & kMain) {
-    fa_status r;
     if (BF16) {
       // fp16 copies of Q and of dO * 2^-e_do for the main kernel's products
+      // (e_do comes from the max |dO| the prepare kernel just recorded)
       const long long n16 = n_vec4 / 2;
       long long cvt_blocks = (n16 + 255) / 256;
       if (cvt_blocks > 148 * 16) cvt_blocks = 148 * 16;
@@ -523,6 +526,9 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
       e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "bwd conversion launch");
     }
+  }
+  if (phases & kMain) {
+    fa_status r;
     if (sparse)
       r = launch_bwd_main_t<D, BF16, false, true>(tq, tk, tv, tdo, a, grid, st);
     else if (causal)
@@ -553,7 +559,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   const long long BHkv = static_cast<long long>(B) * Hkv;
   // each phase reads/writes only some of the tensors
   if (phases & kPrepare) {
-    r = check_ptrs({{o, "o"}, {lse, "lse"}, {dout, "dout"}});
+    r = check_ptrs({{q, "q"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}});
     if (r != FA_OK) return r;
   }
   if (phases & kMain) {
@@ -965,12 +971,11 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
                   block_mask, true, o_res, workspace, workspace_bytes, stream);
 }
 
-fa_status fa_bwd_prepare(const void *o, const void *o_res, const float *lse, const void *dout,
-                         int B, int H, int N, int d, fa_dtype dtype, void *workspace,
+fa_status fa_bwd_prepare(const void *q, const void *o, const void *o_res, const float *lse,
+                         const void *dout, int B, int H, int N, int d, fa_dtype dtype, void *workspace,
                          size_t workspace_bytes, void *stream) {
-  return bwd_impl(nullptr, nullptr, nullptr, o, lse, dout, nullptr, nullptr, nullptr, B, H, N, d,
-                  1.0f, 0, dtype, nullptr, nullptr, false, o_res, workspace, workspace_bytes,
-                  stream, kPrepare);
+  return bwd_impl(q, nullptr, nullptr, o, lse, dout, nullptr, nullptr, nullptr, B, H, N, d, 1.0f, 0,
+                  dtype, nullptr, nullptr, false, o_res, workspace, workspace_bytes, stream, kPrepare);
 }
 
 fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,

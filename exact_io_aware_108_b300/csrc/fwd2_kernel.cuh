@@ -38,6 +38,7 @@
 #pragma once
 #include "common.cuh"
 #include "fwd_kernel.cuh"
+#include "schedule.cuh"
 
 namespace fa {
 
@@ -96,16 +97,9 @@ __global__ void __launch_bounds__(384, 1)
   // while the heads that run concurrently stay few enough for their K and V
   // to stay in L2.
   const int nqb = (a.nqt + 1) >> 1;
-  int bh, qb;
-  {
-    const int BH = static_cast<int>(gridDim.x) / nqb;
-    const int grp = static_cast<int>(blockIdx.x) / (a.hgroup * nqb);
-    const int rem = static_cast<int>(blockIdx.x) - grp * a.hgroup * nqb;
-    const int nh = min(a.hgroup, BH - grp * a.hgroup);
-    qb = rem / nh;
-    bh = grp * a.hgroup + rem % nh;
-  }
-  if (CAUSAL) qb = nqb - 1 - qb;
+  const WorkItem item =
+      grouped_item(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x) / nqb, nqb, a.hgroup, CAUSAL);
+  const int bh = item.bh, qb = item.tile;
   const int b = bh / a.H;
   const int kvh = a.kv_head(bh);
   int kvl = a.N;

@@ -29,6 +29,7 @@
 // TMEM whenever any row of the warp sees a new max.
 #pragma once
 #include "common.cuh"
+#include "schedule.cuh"
 #include "softmax_row.cuh"
 
 namespace fa {
@@ -60,7 +61,7 @@ struct FwdArgs {
   int page_size, pages_per_seq, dec_nq;
 
   // [B*Hkv] index of the key/value head that query head bh ([B*H] index) reads
-  __device__ __forceinline__ int kv_head(int bh) const { return (bh / H) * Hkv + (bh % H) / kv_group; }
+  __device__ __forceinline__ int kv_head(int bh) const { return kv_head_of(bh, H, Hkv); }
 };
 
 template <int D>
@@ -111,9 +112,8 @@ __global__ void __launch_bounds__(256, 1)
 
   // ---- work item: heads are contiguous in the grid so concurrent CTAs share
   // K/V in L2; causal rows run heaviest tile first.
-  const int bh = blockIdx.x / a.nqt;
-  int qt = blockIdx.x % a.nqt;
-  if (CAUSAL) qt = a.nqt - 1 - qt;
+  const WorkItem item = tile_item(static_cast<int>(blockIdx.x), a.nqt, CAUSAL);
+  const int bh = item.bh, qt = item.tile;
   const int b = bh / a.H;
   const int kvh = a.kv_head(bh);
   int kvl = a.N;
@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(256, 1)
   const int n_all = SPARSE ? static_cast<int>(misc[2]) : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
   // split-KV: this CTA's contiguous share [t_lo, t_lo + n_tiles) of the tiles
   const int split = static_cast<int>(blockIdx.y);
-  const int t_lo = static_cast<int>(static_cast<long long>(n_all) * split / a.num_splits);
-  const int n_tiles = static_cast<int>(static_cast<long long>(n_all) * (split + 1) / a.num_splits) - t_lo;
+  int t_lo, n_tiles;
+  split_share(n_all, split, a.num_splits, &t_lo, &n_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

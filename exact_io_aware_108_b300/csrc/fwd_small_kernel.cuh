@@ -46,8 +46,10 @@ struct SmallCfg {
   static constexpr int kBOR = 8;   // P(t) V(t) done
   static constexpr int kBDR = 9;   // drain
   static constexpr int kNumBars = 10;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, list count
+  static constexpr int kListOff = kMiscOff + 16;            // block-sparse: kept key tiles
+  static constexpr int kMaxList = 2048;                     // nkt <= 2048
+  static constexpr int kSmemBytes = kListOff + kMaxList * 2 + 1024;  // + alignment slack
   static constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
   static_assert(kColO + D <= kTmemCols, "TMEM budget");
   // setmaxnreg split: launch with 128 registers x 256 threads (two CTAs per
@@ -58,7 +60,7 @@ struct SmallCfg {
   static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory for two CTAs per SM");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE = false>
 __global__ void __launch_bounds__(256, 2)
     fwd_small_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -74,9 +76,8 @@ __global__ void __launch_bounds__(256, 2)
 
   // ---- work item: heads are contiguous in the grid so concurrent CTAs share
   // K/V in L2; causal rows run heaviest tile first.
-  const int bh = static_cast<int>(blockIdx.x) / a.nqt;
-  int qt = static_cast<int>(blockIdx.x) % a.nqt;
-  if (CAUSAL) qt = a.nqt - 1 - qt;
+  const WorkItem item = tile_item(static_cast<int>(blockIdx.x), a.nqt, CAUSAL);
+  const int bh = item.bh, qt = item.tile;
   const int b = bh / a.H;
   const int kvh = a.kv_head(bh);
   int kvl = a.N;
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(256, 2)
     kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
   }
   const int nkt_eff = (kvl + 127) >> 7;
-  const int n_tiles = CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff;
+  uint16_t *list = reinterpret_cast<uint16_t *>(smem + C::kListOff);
 
   if (tid == 0) {
     mbar_init(bar(C::kBQ), 1);
@@ -108,10 +109,24 @@ __global__ void __launch_bounds__(256, 2)
     tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
     tmem_relinquish();
   }
+  if (SPARSE && warp == 6) {
+    // kept key tiles of this query tile, in increasing order (block-sparse)
+    const uint8_t *mrow = a.block_mask + static_cast<size_t>(qt) * a.nkt;
+    int cnt = 0;
+    for (int j0 = 0; j0 < nkt_eff; j0 += 32) {
+      const int j = j0 + lane;
+      const bool keep = (j < nkt_eff) && (mrow[j] != 0);
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) list[cnt + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(j);
+      cnt += __popc(bal);
+    }
+    if (lane == 0) misc[2] = static_cast<uint32_t>(cnt);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  const int n_tiles = SPARSE ? static_cast<int>(misc[2]) : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
 
   if (warp >= 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
@@ -126,15 +141,16 @@ __global__ void __launch_bounds__(256, 2)
       int nk = 0, nv = 0;
       for (int t = 0; t < n_tiles; ++t) {
         const uint32_t ph = t & 1;  // one stage each: phase = tile parity
+        const int kt = SPARSE ? list[t] : t;
         if (!mbar_wait(bar(C::kBKE), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBKF), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKF), kb * 64, t * 128, kvh, pol_kv);
+          tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKF), kb * 64, kt * 128, kvh, pol_kv);
         nk = t + 1;
         if (!mbar_wait(bar(C::kBVE), ph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBVF), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBVF), kb * 64, t * 128, kvh, pol_kv);
+          tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBVF), kb * 64, kt * 128, kvh, pol_kv);
         nv = t + 1;
       }
       if (*abort_flag) {
@@ -238,8 +254,9 @@ __global__ void __launch_bounds__(256, 2)
         }
       }
       // mask: keys past kv_len / N, and keys after the query on the diagonal
-      int limit = kvl - t * 128;
-      if (CAUSAL && t == qt) limit = min(limit, row + 1);
+      const int kt = SPARSE ? list[t] : t;
+      int limit = kvl - kt * 128;
+      if (CAUSAL && kt == qt) limit = min(limit, row + 1);
       float m_new, alpha;
       const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
       // S(t) complete implies P(t-1) V(t-1) is done (S(t) waited for it): O

@@ -321,18 +321,18 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
  * workspace). Arguments mean what they mean for fa_bwd / fa_bwd_blocksparse.
  *   fa_bwd_prepare  D = rowsum(dO * (O + o_res)) and LSE * log2(e) into the
  *                   workspace; zeroes the workspace's fp32 dQ accumulator;
- *                   records max |dO| and max |D|.
- *   fa_bwd_main     (bf16 inputs: first the fp16 copies of Q and the scaled
- *                   dO into the workspace) one CTA per 128-key tile: dK and
- *                   dV (written directly), dQ partials added into the
- *                   accumulator. block_mask NULL means dense/causal (causal
- *                   applies only then); kv_len must be NULL when block_mask
- *                   is given (FA_ERR_INVALID_ARG otherwise).
+ *                   records max |dO| and max |D|; for bf16 inputs writes the
+ *                   fp16 copies of Q and of the scaled dO into the workspace.
+ *   fa_bwd_main     one CTA per 128-key tile: dK and dV (written directly),
+ *                   dQ partials added into the accumulator. block_mask NULL
+ *                   means dense/causal (causal applies only then); kv_len
+ *                   must be NULL when block_mask is given
+ *                   (FA_ERR_INVALID_ARG otherwise).
  *   fa_bwd_finish   dQ accumulator -> dq (fp16/bf16).
  */
-fa_status fa_bwd_prepare(const void *o, const void *o_res, const float *lse, const void *dout,
-                         int B, int H, int N, int d, fa_dtype dtype, void *workspace,
-                         size_t workspace_bytes, void *stream);
+fa_status fa_bwd_prepare(const void *q, const void *o, const void *o_res, const float *lse,
+                         const void *dout, int B, int H, int N, int d, fa_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream);
 fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
                       void *dv, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, const int32_t *kv_len, const uint8_t *block_mask,

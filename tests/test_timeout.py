@@ -26,11 +26,12 @@ def _starved(fn):
     try:
         out = fn()
         status = fa.fa_get_device_error()
+        message = fa.fa_last_error_message()
     finally:
         assert fa.fa_debug_starve_pipelines(False) == 0
         assert fa.fa_set_wait_limit_ns(0) == 0
     assert status == FA_ERR_TIMEOUT, fa.fa_status_str(status)
-    assert "timed out" in fa.fa_last_error_message()
+    assert "timed out" in message
     assert fa.fa_get_device_error() == 0  # the flag was cleared
     return out
 
