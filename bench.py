@@ -46,7 +46,8 @@ TRAFFIC = {
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
-                  "exact_io_aware_108_b300/csrc/ptx.cuh"]
+                  "exact_io_aware_108_b300/csrc/ptx.cuh",
+                  "exact_io_aware_108_b300/csrc/schedule.cuh"]
 
 
 def kernel_sha():

@@ -181,7 +181,8 @@ fa_status launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 // Returns false (nothing launched) when that check fails.
 template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     const fa::FwdArgs &a, int nqb_grid, cudaStream_t st, fa_status *r) {
+                     const CUtensorMap &to, const CUtensorMap &tr, const fa::FwdArgs &a, int nqb_grid,
+                     cudaStream_t st, fa_status *r) {
   auto kern = fa::fwd2_kernel<D, BF16, CAUSAL, FP8>;
   using C2 = fa::Fwd2Cfg<D, FP8>;
   static std::mutex mu;
@@ -205,7 +206,7 @@ bool try_launch_fwd2(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     *r = cuda_fail(e, "cudaFuncSetAttribute(fwd2)");
     return true;
   }
-  kern<<<nqb_grid, 384, smem, st>>>(tq, tk, tv, a);
+  kern<<<nqb_grid, 384, smem, st>>>(tq, tk, tv, to, tr, a);
   e = cudaGetLastError();
   *r = (e != cudaSuccess) ? cuda_fail(e, "fwd2 launch") : FA_OK;
   return true;
@@ -281,7 +282,8 @@ fa_status launch_merge(const fa::FwdArgs &a, long long rows, int d, cudaStream_t
 
 template <int D, bool BF16>
 fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const fa::FwdArgs &a, int grid, bool causal, bool sparse, cudaStream_t st) {
+                       const CUtensorMap &to, const CUtensorMap &tr, const fa::FwdArgs &a, int grid,
+                       bool causal, bool sparse, cudaStream_t st) {
   fa_status r = FA_OK;
   if (sparse) {
     // block-sparse: one query tile per CTA, two CTAs per SM, each walking
@@ -305,8 +307,8 @@ fa_status launch_fwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   // dense / causal / key padding: two query tiles per CTA
   const long long bh = grid / a.nqt;
   const int grid2 = static_cast<int>(bh * ((a.nqt + 1) / 2));
-  if (causal ? try_launch_fwd2<D, BF16, true>(tq, tk, tv, a, grid2, st, &r)
-             : try_launch_fwd2<D, BF16, false>(tq, tk, tv, a, grid2, st, &r))
+  if (causal ? try_launch_fwd2<D, BF16, true>(tq, tk, tv, to, tr, a, grid2, st, &r)
+             : try_launch_fwd2<D, BF16, false>(tq, tk, tv, to, tr, a, grid2, st, &r))
     return r;
   if (causal) return launch_fwd_t<D, BF16, true, false>(tq, tk, tv, a, grid, st);
   return launch_fwd_t<D, BF16, false, false>(tq, tk, tv, a, grid, st);
@@ -418,6 +420,10 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   if ((r = make_tile_map(&tq, q, dt, N, s.BH, d, "q")) != FA_OK) return r;
   if ((r = make_tile_map(&tk, k, dt, N, BHkv, d, "k")) != FA_OK) return r;
   if ((r = make_tile_map(&tv, v, dt, N, BHkv, d, "v")) != FA_OK) return r;
+  // O and its residual, stored by the two-tile kernel through TMA
+  CUtensorMap to, tr;
+  if ((r = make_tile_map(&to, o, dt, N, s.BH, d, "o")) != FA_OK) return r;
+  if ((r = make_tile_map(&tr, o_res != nullptr ? o_res : o, dt, N, s.BH, d, "o_res")) != FA_OK) return r;
   fa::FwdArgs a;
   a.o = o;
   a.o_res = o_res;
@@ -442,11 +448,11 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
   if (d == 64)
-    r = dt == FA_BF16 ? launch_fwd_d<64, true>(tq, tk, tv, a, grid, c, sparse, st)
-                      : launch_fwd_d<64, false>(tq, tk, tv, a, grid, c, sparse, st);
+    r = dt == FA_BF16 ? launch_fwd_d<64, true>(tq, tk, tv, to, tr, a, grid, c, sparse, st)
+                      : launch_fwd_d<64, false>(tq, tk, tv, to, tr, a, grid, c, sparse, st);
   else
-    r = dt == FA_BF16 ? launch_fwd_d<128, true>(tq, tk, tv, a, grid, c, sparse, st)
-                      : launch_fwd_d<128, false>(tq, tk, tv, a, grid, c, sparse, st);
+    r = dt == FA_BF16 ? launch_fwd_d<128, true>(tq, tk, tv, to, tr, a, grid, c, sparse, st)
+                      : launch_fwd_d<128, false>(tq, tk, tv, to, tr, a, grid, c, sparse, st);
   if (r != FA_OK) return r;
   return ok();
 }
@@ -845,8 +851,9 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   const int grid2 = static_cast<int>(s.BH * ((s.nqt + 1) / 2));
-  const bool launched = causal ? try_launch_fwd2<128, true, true, true>(tq, tk, tv, a, grid2, st, &r)
-                               : try_launch_fwd2<128, true, false, true>(tq, tk, tv, a, grid2, st, &r);
+  // (the 8-bit instance stores O with plain stores; its O map is not read)
+  const bool launched = causal ? try_launch_fwd2<128, true, true, true>(tq, tk, tv, tq, tq, a, grid2, st, &r)
+                               : try_launch_fwd2<128, true, false, true>(tq, tk, tv, tq, tq, a, grid2, st, &r);
   if (!launched) return fail(FA_ERR_CUDA, "8-bit forward: kernel register count differs from its warpgroup split");
   if (r != FA_OK) return r;
   return ok();

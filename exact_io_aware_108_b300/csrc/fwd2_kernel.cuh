@@ -76,10 +76,14 @@ struct Fwd2Cfg {
   static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kLaunchRegs * 384, "register split");
 };
 
+// tm_o, tm_r: O and its rounding residual as [B*H][N][D] 16-bit tensors
+// with the same 64 x 128 x 1 boxes as Q (tm_r is only used when a.o_res is
+// set; the 8-bit forward stores O directly).
 template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const __grid_constant__ CUtensorMap tm_r, const FwdArgs a) {
   static_assert(!FP8 || BF16, "8-bit inputs give bf16 O");
   using C = Fwd2Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw2[];
@@ -389,8 +393,6 @@ __global__ void __launch_bounds__(384, 1)
     if (qt < a.nqt) {
       // 8-bit inputs: O carries V's dequantisation factor
       const float inv_l = (l > 0.f) ? (FP8 ? a.o_scale : 1.f) / l : 0.f;
-      uint16_t *orow = static_cast<uint16_t *>(a.o) +
-                       (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
       uint32_t oall[D / 32][32];
       if (have_o) {
 #pragma unroll
@@ -404,29 +406,67 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) oall[j][i] = 0u;
       }
+      if constexpr (FP8) {
+        uint16_t *orow = static_cast<uint16_t *>(a.o) +
+                         (static_cast<size_t>(bh) * a.N + static_cast<size_t>(q_row)) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        const uint32_t (&o)[32] = oall[c0 / 32];
-        uint32_t pk[16], rk[16];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          const uint32_t (&o)[32] = oall[c0 / 32];
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
-          pk[i] = pack2<BF16>(x0, x1);
-          rk[i] = pack2<BF16>(x0 - unpack_lo<BF16>(pk[i]), x1 - unpack_hi<BF16>(pk[i]));
-        }
-        if (q_row < a.N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          if (a.o_res != nullptr) {
-            uint4 *dr = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.o_res) +
-                                                  (orow - static_cast<uint16_t *>(a.o)) + c0);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (q_row < a.N) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-              dr[v] = make_uint4(rk[4 * v], rk[4 * v + 1], rk[4 * v + 2], rk[4 * v + 3]);
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
+      } else {
+        // O (then its residual) goes through the Q_x tile, free once the last
+        // P_x V is done (every S_x product was issued before it), in the
+        // 128-byte-swizzled box layout of the tensor map, and leaves by TMA
+        // stores: the CTA waits only until the boxes are read, not written.
+        // Rows past N are outside the tensor and are not written.
+        const uint32_t stage = sbase + C::kQOff + x * C::kTileBytes;
+        const bool res = a.o_res != nullptr;
+        for (int pass = 0; pass < (res ? 2 : 1); ++pass) {
+          if (pass == 1) {  // the O boxes must have been read before the residual overwrites them
+            if (row == 0) bulk_wait_read0();
+            named_bar_sync(2 + x, 128);
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            const uint32_t (&o)[32] = oall[c0 / 32];
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+              const uint32_t pk = pack2<BF16>(x0, x1);
+              w[i] = pass == 0 ? pk : pack2<BF16>(x0 - unpack_lo<BF16>(pk), x1 - unpack_hi<BF16>(pk));
+            }
+            // columns c0 .. c0 + 31 are 16-byte chunks 4 (c0 % 64) / 32 .. +3
+            // of this row in box c0 / 64
+            const uint32_t rbase = stage + (c0 / 64) * 16384 + row * 128;
+            const int ch0 = (c0 % 64) / 8;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               rbase + (static_cast<uint32_t>((ch0 + v) ^ (row & 7)) << 4)),
+                           "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3])
+                           : "memory");
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(2 + x, 128);
+          if (row == 0) {
+#pragma unroll
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_store_3d(pass == 0 ? &tm_o : &tm_r, stage + kb * 16384, kb * 64, qt * 128, bh);
+            bulk_commit();
+          }
+        }
+        if (row == 0) bulk_wait_read0();
       }
       if (q_row < a.N)
         a.lse[static_cast<size_t>(bh) * a.N + q_row] =
