@@ -99,7 +99,11 @@ def test_gqa_sharp_equals_plain_path_on_repeated_kv():
     torch.cuda.synchronize()
     assert fa.fa_get_device_error() == 0
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
-    assert (dq.float() - dq2.float()).abs().max().item() <= 1e-3
+    # dQ sums key tiles with fp32 atomics in no fixed order: the fp32 sums
+    # agree to ~1e-6 relative, and their 16-bit roundings to within one ulp
+    dq_a, dq_b = dq.cpu().double().numpy(), dq2.cpu().double().numpy()
+    one_ulp = 2 * half_ulp(np.maximum(np.abs(dq_a), np.abs(dq_b)), torch.bfloat16)
+    assert np.all(np.abs(dq_a - dq_b) <= one_ulp + 1e-4)
     for name, g, p in (("dK", dk, dk2), ("dV", dv, dv2)):
         per_head = p.cpu().double().numpy().reshape(3, 2, 2, 320, 128)
         p_sum = per_head.sum(axis=2)
@@ -128,7 +132,9 @@ def test_gqa_with_hkv_equal_h_is_the_plain_path():
     fa.fa_bwd_gqa(q, k, v, o1, l1, do, *g2, scale, True, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
-    check("dQ", g2[0].cpu(), g1[0].cpu().double().numpy(), 1e-3, q.dtype)
+    # dQ: fp32 atomics in no fixed order; the 16-bit results agree to one ulp
+    a_, b_ = g2[0].cpu().double().numpy(), g1[0].cpu().double().numpy()
+    assert np.all(np.abs(a_ - b_) <= 2 * half_ulp(np.maximum(np.abs(a_), np.abs(b_)), q.dtype) + 1e-4)
 
 
 def test_gqa_full_size_whole_heads():
