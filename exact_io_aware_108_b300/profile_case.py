@@ -11,7 +11,10 @@ only, the inference forward).
         --ctx 4096 8192 --page-size 16 --splits 0 --iters 2
 
 runs the paged decode instead (one new token per sequence, --nq for more);
---fp8 runs the 8-bit forward on e4m3 inputs of the given shape (d = 128).
+--fp8 runs the 8-bit forward on e4m3 inputs of the given shape (d = 128);
+--block-sparse P the block-sparse forward and backward (mask as in the
+benchmark's block-sparse workload: tiles kept with probability P, seed 7,
+diagonal kept).
 """
 from __future__ import annotations
 
@@ -42,6 +45,8 @@ def main():
     ap.add_argument("--page-size", type=int, default=16)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--fp8", action="store_true", help="8-bit forward")
+    ap.add_argument("--block-sparse", type=float, default=None, metavar="P",
+                    help="block-sparse: 128x128 tiles kept with probability P (seed 7) plus the diagonal")
     a = ap.parse_args()
     if a.decode:
         return decode(a)
@@ -56,14 +61,21 @@ def main():
     do = torch.randn(shape, device="cuda", generator=g).to(dt)
     scale = 1.0 / math.sqrt(a.d)
     ws = torch.empty(fa.fa_bwd_workspace_size(*shape), dtype=torch.uint8, device="cuda")
+    bm = None
+    if a.block_sparse is not None:
+        from exact_io_aware_108_b300 import inputs
+        bm = inputs.make_block_mask(a.N, a.block_sparse, seed=7).cuda()
+    causal = a.causal and bm is None
     for _ in range(a.iters):
         if a.plain:
-            o, lse = fa.attention_forward(q, k, v, scale, a.causal)
+            o, lse = fa.attention_forward(q, k, v, scale, causal, block_mask=bm)
             o_res = None
         else:
-            o, lse, o_res = fa.attention_forward(q, k, v, scale, a.causal, return_residual=True)
+            o, lse, o_res = fa.attention_forward(q, k, v, scale, causal, block_mask=bm,
+                                                 return_residual=True)
         if not a.fwd_only:
-            fa.attention_backward(q, k, v, o, lse, do, scale, a.causal, o_res=o_res, workspace=ws)
+            fa.attention_backward(q, k, v, o, lse, do, scale, causal, block_mask=bm, o_res=o_res,
+                                  workspace=ws)
     torch.cuda.synchronize()
     assert fa.fa_get_device_error() == 0, "device error"
     print("ok", shape, a.dtype, "causal" if a.causal else "dense")
