@@ -113,6 +113,18 @@ int head_group(int N, int d, bool causal) {
   return static_cast<int>(g < 1 ? 1 : (g > 16 ? 16 : g));
 }
 
+// The two-tile forward's group: the largest power of two heads within the
+// 48 MB rule and at most 8. Measured on the long-context sweep (B * N =
+// 32768, H = 16, d = 128): groups of 8 against the rule's 16 / 12 / 6 heads
+// at N = 4096 / 8192 / 16384 ran equal / 2 % / 4 % faster; a group size
+// that leaves a short last group costs.
+int fwd_head_group(int N, int d, bool causal) {
+  const int g = head_group(N, d, causal);
+  int p = 1;
+  while (p * 2 <= g && p * 2 <= 8) p *= 2;
+  return p;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Shape {
@@ -434,7 +446,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.N = N;
   a.nqt = s.nqt;
   a.nkt = s.nqt;
-  a.hgroup = head_group(N, d, causal != 0);
+  a.hgroup = fwd_head_group(N, d, causal != 0);
   a.Hkv = Hkv;
   a.kv_group = H / Hkv;
   a.num_splits = S;

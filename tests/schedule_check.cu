@@ -31,6 +31,14 @@ static int head_group(int N, int d, bool causal) {
   return static_cast<int>(g < 1 ? 1 : (g > 16 ? 16 : g));
 }
 
+// the two-tile forward's group: a power of two within the rule, at most 8
+static int fwd_head_group(int N, int d, bool causal) {
+  const int g = head_group(N, d, causal);
+  int p = 1;
+  while (p * 2 <= g && p * 2 <= 8) p *= 2;
+  return p;
+}
+
 static void check_grouped(int n_heads, int n_tiles, int hgroup, bool reverse, const char *what) {
   std::vector<int> seen(static_cast<size_t>(n_heads) * n_tiles, 0);
   for (int blk = 0; blk < n_heads * n_tiles; ++blk) {
@@ -104,7 +112,7 @@ int main() {
     for (int causal = 0; causal < 2; ++causal) {
       const int hg = head_group(s.N, s.d, causal);
       // two-tile forward: query-tile pairs of B*H heads
-      check_grouped(s.B * s.H, nqb, hg, causal, "two-tile forward");
+      check_grouped(s.B * s.H, nqb, fwd_head_group(s.N, s.d, causal), causal, "two-tile forward");
       // backward: key tiles of B*Hkv heads (group size divided by the query heads per key/value head)
       int hgb = hg / (s.H / s.Hkv);
       if (hgb < 1) hgb = 1;
