@@ -188,7 +188,7 @@ class Problem:
                      o_res=self.o_res, stream=stream)
         if fwd_events is not None:
             fwd_events[1].record(stream)
-        fa.fa_bwd_prepare(d["q"], self.o, self.o_res, self.lse, d["dout"], self.ws, stream=stream)
+        fa.fa_bwd_prepare(d["q"], d["v"], self.o, self.o_res, self.lse, d["dout"], self.ws, stream=stream)
         if main_events is not None:
             main_events[0].record(stream)
         fa.fa_bwd_main(d["q"], d["k"], d["v"], d["dout"], self.dk, self.dv, w.scale, w.causal,

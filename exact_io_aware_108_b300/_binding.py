@@ -88,7 +88,7 @@ def load_library():
         lib.fa_bwd.argtypes = bwd + [_i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_blocksparse.argtypes = bwd + [_i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_gqa.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
-        lib.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd_main.argtypes = [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]
         lib.fa_bwd_finish.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd_noalloc.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp, _vp]
@@ -304,9 +304,9 @@ def _ws_bytes(workspace, workspace_bytes):
     return int(workspace_bytes)
 
 
-def fa_bwd_prepare(q, o, o_res, lse, dout, workspace, workspace_bytes=None, stream=None):
+def fa_bwd_prepare(q, v, o, o_res, lse, dout, workspace, workspace_bytes=None, stream=None):
     B, H, N, d = _dims(o)
-    _check(load_library().fa_bwd_prepare(_ptr(q), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(dout), B, H, N,
+    _check(load_library().fa_bwd_prepare(_ptr(q), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(dout), B, H, N,
                                          d, _dtype_code(o), _ptr(workspace),
                                          _ws_bytes(workspace, workspace_bytes), _stream(stream)),
            "fa_bwd_prepare")

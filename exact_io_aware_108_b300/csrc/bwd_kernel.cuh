@@ -23,17 +23,18 @@
 //             largest element lands in [2^14, 2^15): gradients of any
 //             magnitude keep fp16's full precision. dP and dV are
 //             multiplied back by 2^e_do in fp32 (exact).
-//   dS        stored as dS * scale * 2^-e_s, e_s chosen per CTA from the
-//             bound |dS| <= |dP| + |D| <= d max|dO| max|V_j| + max|D| so the
-//             largest possible value stays below 2^15; dQ and dK partials are
-//             multiplied back by 2^e_s in fp32 (exact).
+//   dS        stored as dS * scale * 2^-e_s, one e_s per call from the
+//             bound |dS| <= |dP| + |D| <= d max|dO| max|V| + max|D| so the
+//             largest possible value stays below 2^15; dK is multiplied back
+//             by 2^e_s in its epilogue, dQ when its fp32 accumulator is
+//             converted to 16 bits (both exact).
 // For fp16 inputs only the dS scaling applies.
 //
 // Kernels:
 //   bwd_pre_kernel   -scale * D_i and -LSE_i * log2(e) per query row (padded
 //                    to whole 128-row tiles; pad rows get D = 0, LSE = +inf so
 //                    P = 0), zeroes the fp32 dQ accumulator, and records
-//                    max |dO| and max |D| for the scaling above. D_i = dO_i .
+//                    max |dO|, max |D| and max |V| for the scaling above. D_i = dO_i .
 //                    O_i uses O plus its rounding residual when the forward
 //                    wrote one: with bf16 O alone the rounding of O moves D_i
 //                    by up to ~0.05 at d = 128, which reaches dQ and dK.
@@ -54,8 +55,7 @@
 //   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
 //                   query tile i through a two-stage ring.
 //   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
-//   warpgroups 1-3  at the start: K_j, V_j -> fp16 in place (bf16 inputs),
-//                   max |V_j| and e_s.
+//   warpgroups 1-3  at the start: K_j, V_j -> fp16 in place (bf16 inputs).
 //   warpgroups 1, 2 one 64-query half h of the tile each: P^T -> TMEM
 //                   (fp16), dS^T -> shared memory (fp16, scale and 2^-e_s
 //                   folded in, computed from the fp32 P). A thread holds 4
@@ -63,8 +63,8 @@
 //                   16 of the half's per-query LSE and D values; at the end
 //                   warpgroup 1 writes dK, warpgroup 2 writes dV (one key
 //                   row per thread).
-//   warpgroup 3     reads the dQ partial from TMEM and adds it, times 2^e_s,
-//                   to the fp32 accumulator (d = 128: thread r owns head-dim
+//   warpgroup 3     reads the dQ partial from TMEM and adds it to the fp32
+//                   accumulator (d = 128: thread r owns head-dim
 //                   channel r of the transposed partial; d = 64: thread r
 //                   owns query r).
 // The MMA issue order per query tile i is dP_i, dV_i, dQ_i, S_{i+1}, dK_i
@@ -96,9 +96,13 @@ struct BwdArgs {
   // written by bwd_cvt_kernel) and the sources they are made from
   const void *q;
   void *q16, *do16;
-  // [0] max |dO| and [1] max |D| as fp32 bit patterns (non-negative floats
-  // order like their bits), zeroed before bwd_pre_kernel
+  // [0] max |dO|, [1] max |D|, [2] max |V| as fp32 bit patterns
+  // (non-negative floats order like their bits), zeroed before
+  // bwd_pre_kernel; [3] the dS exponent e_s, written by the main kernel for
+  // the dQ conversion
   unsigned int *stats;
+  const void *v;     // V, read by bwd_pre_kernel for max |V|
+  long long n_v16;   // 16-byte chunks of V
   int H, N, nqt, nkt;
   int hgroup;    // heads per scheduling group (causal launch order, see below)
   int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
@@ -133,6 +137,18 @@ __device__ __forceinline__ int scale_exponent(float x, int top) {
 // Exponent of the dO scaling: max |dO| * 2^-e_do in [2^14, 2^15).
 __device__ __forceinline__ int do_exponent(const unsigned int *stats) {
   return scale_exponent(__uint_as_float(stats[0]), 15);
+}
+
+// Exponent of the dS scaling (dS is stored as dS * scale * 2^-e_s): from
+// |dS| <= |dP| + |D| <= d max|dO| max|V| + max|D|, the largest possible
+// stored value stays below 2^15. One value for the whole call, so the fp32
+// dQ accumulator holds dQ * 2^-e_s and the conversion to 16 bits multiplies
+// it back. Clamped values are at most 65504, so the bound stays finite for
+// finite inputs.
+__device__ __forceinline__ int ds_exponent(const unsigned int *stats, float scale, int d) {
+  const float amax_do = __uint_as_float(stats[0]), amax_d = __uint_as_float(stats[1]);
+  const float amax_v = fminf(__uint_as_float(stats[2]), 65504.f);
+  return scale_exponent(scale * (static_cast<float>(d) * amax_do * amax_v + amax_d), 15);
 }
 
 // Eight bf16 values (16 bytes) -> eight fp16 values, rounded to nearest and
@@ -178,7 +194,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long rows_pad) {
   constexpr int LPR = D / 8;         // lanes per row (8 elements each)
   constexpr int RPW = 32 / LPR;      // rows per warp step
-  __shared__ float red[2][8];
+  __shared__ float red[3][8];
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR, grp = lane / LPR;
   const long long tile_rows = static_cast<long long>(a.nqt) * 128;
@@ -231,8 +247,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
       a.lse_l2[row] = nl;
     }
   }
+  // max |V| (bf16 V is converted to fp16 by the main kernel; either type
+  // needs it for the dS exponent)
+  float amax_v = 0.f;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < a.n_v16;
+       g += static_cast<long long>(gridDim.x) * blockDim.x)
+    amax_v = fmaxf(amax_v, amax16x8<BF16>(reinterpret_cast<const uint4 *>(a.v)[g]));
   block_max_to(a.stats + 0, amax_do, red[0]);
   block_max_to(a.stats + 1, amax_d, red[1]);
+  block_max_to(a.stats + 2, amax_v, red[2]);
 }
 
 // ----------------------------------------------------------------- fp16 copies
@@ -261,8 +284,10 @@ __global__ void __launch_bounds__(256) bwd_cvt_kernel(const BwdArgs a, long long
 // ----------------------------------------------------------------- dq convert
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdArgs a, long long n_vec4, int D) {
-  // n_vec4 = BH * N * D / 4 output groups of 4 elements
+  // n_vec4 = BH * N * D / 4 output groups of 4 elements; the accumulator
+  // holds dQ * 2^-e_s (e_s as the main kernel recorded it)
   const long long tile_rows = static_cast<long long>(a.nqt) * 128;
+  const float u_s = exp2i(static_cast<int>(a.stats[3]));
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_vec4;
        g += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long e = g * 4;
@@ -270,8 +295,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdArgs a, long long 
     const long long bh = row / a.N, i = row % a.N;
     const float4 v = *reinterpret_cast<const float4 *>(a.dq_acc + (bh * tile_rows + i) * D + c);
     uint2 out;
-    out.x = pack2<BF16>(v.x, v.y);
-    out.y = pack2<BF16>(v.z, v.w);
+    out.x = pack2<BF16>(v.x * u_s, v.y * u_s);
+    out.y = pack2<BF16>(v.z * u_s, v.w * u_s);
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.dq) + e) = out;
   }
 }
@@ -292,7 +317,7 @@ struct BwdCfg {
   static constexpr int kBKV = 0, kBQF = 1, kBQE = 3, kBSF = 5, kBDPF = 6, kBPR = 7 /* x2 */,
                        kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13, kBDSF = 14,
                        kBCK = 15 /* K ready in fp16, 384 arrivals */,
-                       kBCV = 16 /* V ready in fp16, max |V_j| slots written, 384 arrivals */,
+                       kBCV = 16 /* V ready in fp16, 384 arrivals */,
                        kNumBars = 17;
   // d = 128: the dQ partial is computed transposed (dQ^T = K^T dS^T, TMEM
   // lane = head-dim channel, column = query) so one warp's reduction into
@@ -300,9 +325,8 @@ struct BwdCfg {
   // 128-byte line per instruction instead of 32 scattered 16-byte pieces.
   static constexpr bool kDqT = (D == 128);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // misc: [0] TMEM address, [1] abort flag, [4, 16) per-warp max |V| of
-  // warpgroups 1-3 (fp32)
-  static constexpr int kSmemBytes = kMiscOff + 64;
+  // misc: [0] TMEM address, [1] abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr uint32_t kColDQ = kDqT ? kColDP : 2 * D + 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -379,6 +403,7 @@ __global__ void __launch_bounds__(512, 1)
     }
   };
 
+  if (blockIdx.x == 0 && tid == 0) a.stats[3] = static_cast<unsigned int>(ds_exponent(a.stats, a.scale, D));
   if (tid == 0) {
     mbar_init(bar(C::kBKV), 1);
     for (int s = 0; s < 2; ++s) {
@@ -469,7 +494,9 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(bar(C::kBSF));
       };
-      bool ok = mbar_wait(bar(C::kBCK), 0, abort_flag) && mbar_wait(bar(C::kBQF), 0, abort_flag);
+      // K and V landed, and (bf16 inputs) K converted
+      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag) && mbar_wait(bar(C::kBCK), 0, abort_flag) &&
+                mbar_wait(bar(C::kBQF), 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -560,60 +587,38 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // ---- prologue of warpgroups 1-3: K_j -> fp16 in place (bf16 inputs),
-    // then V_j and its max |V_j| per warp into shared memory. The first S^T
-    // needs only K; the first dP^T and the dS exponent wait for V.
-    float *slots = reinterpret_cast<float *>(misc + 4);
+    // ---- prologue of warpgroups 1-3 (bf16 inputs): K_j, then V_j -> fp16
+    // in place. The first S^T needs only K; the first dP^T waits for V.
     if (n_iter > 0) {
       constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
-      float amax_v = 0.f, amax_k = 0.f;
-      const bool landed = mbar_wait_warp(bar(C::kBKV), 0, abort_flag);
-      if (BF16 && landed) {
+      float amax = 0.f;
+      const bool landed = BF16 && mbar_wait_warp(bar(C::kBKV), 0, abort_flag);
+      if (landed) {
         uint4 *kt16 = reinterpret_cast<uint4 *>(smem + C::kKOff);
-        for (int c = tid - 128; c < kChunks; c += 384) kt16[c] = bf16x8_to_f16x8(kt16[c], amax_k);
+        for (int c = tid - 128; c < kChunks; c += 384) kt16[c] = bf16x8_to_f16x8(kt16[c], amax);
         fence_proxy_async_smem();
       }
       tc_fence_before();
       mbar_arrive(bar(C::kBCK));
       if (landed) {
         uint4 *vt16 = reinterpret_cast<uint4 *>(smem + C::kVOff);
-        for (int c = tid - 128; c < kChunks; c += 384) {
-          if constexpr (BF16)
-            vt16[c] = bf16x8_to_f16x8(vt16[c], amax_v);
-          else
-            amax_v = fmaxf(amax_v, amax16x8<false>(vt16[c]));
-        }
-        if (BF16 && fmaxf(amax_k, amax_v) > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
-        if (BF16) fence_proxy_async_smem();
+        for (int c = tid - 128; c < kChunks; c += 384) vt16[c] = bf16x8_to_f16x8(vt16[c], amax);
+        if (amax > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
+        fence_proxy_async_smem();
       }
-#pragma unroll
-      for (int s2 = 16; s2 > 0; s2 >>= 1) amax_v = fmaxf(amax_v, __shfl_xor_sync(0xffffffffu, amax_v, s2));
-      if (lane == 0) slots[warp - 4] = amax_v;
-      __syncwarp();
       tc_fence_before();
       mbar_arrive(bar(C::kBCV));
-      // every thread of warpgroups 1-3 reads the slots (the dS exponent) next
-      mbar_wait_warp(bar(C::kBCV), 0, abort_flag);
     }
-    // e_s: |dS| <= |dP| + |D| <= d max|dO| max|V_j| + max|D| (clamped values
-    // are at most 65504, so the bound stays finite for finite inputs); dS is
-    // stored times scale 2^-e_s. e_do: dO16 = dO 2^-e_do.
-    auto exponent_s = [&]() -> int {
-      float amax_v = 0.f;
-#pragma unroll
-      for (int w = 0; w < 12; ++w) amax_v = fmaxf(amax_v, slots[w]);
-      const float amax_do = __uint_as_float(a.stats[0]), amax_d = __uint_as_float(a.stats[1]);
-      return scale_exponent(a.scale * (static_cast<float>(D) * amax_do * fminf(amax_v, 65504.f) + amax_d), 15);
-    };
-    auto exponent_do = [&]() -> int { return BF16 ? do_exponent(a.stats) : 0; };
+    const int e_s = ds_exponent(a.stats, a.scale, D);
+    const int e_do = BF16 ? do_exponent(a.stats) : 0;
     if (warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T, one query half
     const int h = (warp >> 2) - 1;  // query half: columns [64h, 64h+64) of the tile
     const int r = tid & 127;         // key row of this thread's lane (epilogue)
     const int key = kt * 128 + r;
     const float sl2 = a.scale_log2;
-    const float f_s = n_iter > 0 ? exp2i(-exponent_s()) : 1.f;
-    const float sc_dp = a.scale * f_s * exp2i(exponent_do());
+    const float f_s = exp2i(-e_s);
+    const float sc_dp = a.scale * f_s * exp2i(e_do);
     // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
     // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
     // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (key < a.N) {
       // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO)
-      const float u = exp2i(h == 0 ? (n_iter > 0 ? exponent_s() : 0) : exponent_do());
+      const float u = exp2i(h == 0 ? e_s : e_do);
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
@@ -766,7 +771,6 @@ __global__ void __launch_bounds__(512, 1)
     } else {
     // ------------------------------------------------------------ dQ partials
     const int r = tid & 127;  // d = 128: head-dim channel; d = 64: query row
-    const float u_s = n_iter > 0 ? exp2i(exponent_s()) : 1.f;  // the partial carries 2^-e_s
     int g = 0, qi = q_first;
     for (int u = 0; u < n_iter; ++u) {
       if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
@@ -794,7 +798,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int j = 0; j < 4; ++j)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]) * u_s);
+            atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]));
             if ((i & 15) == 15) {
               const long long t0 = clock64();
               while (clock64() - t0 < 120) {
@@ -808,8 +812,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             atomicAdd(reinterpret_cast<float4 *>(acc + j * 32 + i),
-                      make_float4(__uint_as_float(v[j][i]) * u_s, __uint_as_float(v[j][i + 1]) * u_s,
-                                  __uint_as_float(v[j][i + 2]) * u_s, __uint_as_float(v[j][i + 3]) * u_s));
+                      make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
+                                  __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
       }
       advance(g, qi);
     }

@@ -526,7 +526,7 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        cudaStream_t st) {
   cudaError_t e;
   if (phases & kPrepare) {
-    e = cudaMemsetAsync(a.stats, 0, 2 * sizeof(unsigned int), st);
+    e = cudaMemsetAsync(a.stats, 0, 4 * sizeof(unsigned int), st);
     if (e != cudaSuccess) return cuda_fail(e, "bwd statistics reset");
     constexpr int rows_per_block = 8 * (32 / (D / 8));
     long long pre_blocks = (rows_pad + rows_per_block - 1) / rows_per_block;
@@ -577,7 +577,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   const long long BHkv = static_cast<long long>(B) * Hkv;
   // each phase reads/writes only some of the tensors
   if (phases & kPrepare) {
-    r = check_ptrs({{q, "q"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}});
+    r = check_ptrs({{q, "q"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}});
     if (r != FA_OK) return r;
   }
   if (phases & kMain) {
@@ -636,6 +636,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.q16 = q16;
   a.do16 = do16;
   a.stats = stats;
+  a.v = v;
+  a.n_v16 = BHkv * static_cast<long long>(N) * d / 8;
   a.dq_acc = reinterpret_cast<float *>(ws + 2 * up256(rows * 4));
   a.kv_len = kv_len;
   a.block_mask = block_mask;
@@ -643,6 +645,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.q16 = q16;
   a.do16 = do16;
   a.stats = stats;
+  a.v = v;
+  a.n_v16 = BHkv * static_cast<long long>(N) * d / 8;
   a.H = H;
   a.N = N;
   a.nqt = s.nqt;
@@ -990,10 +994,10 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
                   block_mask, true, o_res, workspace, workspace_bytes, stream);
 }
 
-fa_status fa_bwd_prepare(const void *q, const void *o, const void *o_res, const float *lse,
-                         const void *dout, int B, int H, int N, int d, fa_dtype dtype, void *workspace,
-                         size_t workspace_bytes, void *stream) {
-  return bwd_impl(q, nullptr, nullptr, o, lse, dout, nullptr, nullptr, nullptr, B, H, N, d, 1.0f, 0,
+fa_status fa_bwd_prepare(const void *q, const void *v, const void *o, const void *o_res,
+                         const float *lse, const void *dout, int B, int H, int N, int d, fa_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, nullptr, v, o, lse, dout, nullptr, nullptr, nullptr, B, H, N, d, 1.0f, 0,
                   dtype, nullptr, nullptr, false, o_res, workspace, workspace_bytes, stream, kPrepare);
 }
 

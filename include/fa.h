@@ -266,7 +266,7 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int causal, int
  * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
  * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ
  * accumulator [R, d], each rounded up to 256 bytes; 256 bytes of statistics
- * (max |dO|, max |D|); then room for fp16 copies of Q and of the scaled dO
+ * (max |dO|, max |D|, max |V|, the dS exponent); then room for fp16 copies of Q and of the scaled dO
  * ([B, H, N, d] each, rounded up to 256 bytes; used for bf16 inputs only).
  * Returns 0 for invalid sizes.
  */
@@ -321,8 +321,9 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
  * workspace). Arguments mean what they mean for fa_bwd / fa_bwd_blocksparse.
  *   fa_bwd_prepare  D = rowsum(dO * (O + o_res)) and LSE * log2(e) into the
  *                   workspace; zeroes the workspace's fp32 dQ accumulator;
- *                   records max |dO| and max |D|; for bf16 inputs writes the
- *                   fp16 copies of Q and of the scaled dO into the workspace.
+ *                   records max |dO|, max |D| and max |V|; for bf16 inputs
+ *                   writes the fp16 copies of Q and of the scaled dO into the
+ *                   workspace.
  *   fa_bwd_main     one CTA per 128-key tile: dK and dV (written directly),
  *                   dQ partials added into the accumulator. block_mask NULL
  *                   means dense/causal (causal applies only then); kv_len
@@ -330,9 +331,9 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
  *                   (FA_ERR_INVALID_ARG otherwise).
  *   fa_bwd_finish   dQ accumulator -> dq (fp16/bf16).
  */
-fa_status fa_bwd_prepare(const void *q, const void *o, const void *o_res, const float *lse,
-                         const void *dout, int B, int H, int N, int d, fa_dtype dtype,
-                         void *workspace, size_t workspace_bytes, void *stream);
+fa_status fa_bwd_prepare(const void *q, const void *v, const void *o, const void *o_res,
+                         const float *lse, const void *dout, int B, int H, int N, int d,
+                         fa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
 fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
                       void *dv, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, const int32_t *kv_len, const uint8_t *block_mask,
