@@ -158,3 +158,28 @@ def test_bwd_full_size_every_head_sampled(name):
     worst = check_bwd_every_head(t, w, dq, dk, dv)
     print(f"\n{name}: max |d grad| over sampled rows of every head: "
           + ", ".join(f"{k} {v:.4g}" for k, v in worst.items()))
+
+
+@pytest.mark.parametrize("dt,causal", [("bf16", True), ("f16", False)])
+def test_bwd_three_phases_equal_fa_bwd(dt, causal):
+    """fa_bwd_prepare, fa_bwd_main and fa_bwd_finish called one by one give
+    what fa_bwd gives: dK and dV bitwise, dQ (fp32 atomics in no fixed
+    order) to one 16-bit ulp."""
+    import exact_io_aware_108_b300 as fa
+    from tests.tolerance import half_ulp
+    t = inputs.make_qkv(2, 3, 600, 128, dt, seed=44, qk_mult=2.0)
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "dout"))
+    scale = 1.0 / math.sqrt(128)
+    o, lse, res = fa.attention_forward(q, k, v, scale, causal=causal, return_residual=True)
+    ws = torch.empty(fa.fa_bwd_workspace_size(2, 3, 600, 128), dtype=torch.uint8, device="cuda")
+    g1 = [torch.empty_like(q) for _ in range(3)]
+    fa.fa_bwd(q, k, v, o, lse, do, *g1, scale, causal, None, res, ws)
+    g2 = [torch.full_like(q, float("nan")) for _ in range(3)]
+    fa.fa_bwd_prepare(q, v, o, res, lse, do, ws)
+    fa.fa_bwd_main(q, k, v, do, g2[1], g2[2], scale, causal, workspace=ws)
+    fa.fa_bwd_finish(g2[0], ws)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    a_, b_ = g1[0].cpu().double().numpy(), g2[0].cpu().double().numpy()
+    assert np.all(np.abs(a_ - b_) <= 2 * half_ulp(np.maximum(np.abs(a_), np.abs(b_)), q.dtype) + 1e-4)
