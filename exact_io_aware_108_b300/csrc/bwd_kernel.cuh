@@ -31,7 +31,7 @@
 // For fp16 inputs only the dS scaling applies.
 //
 // Kernels:
-//   bwd_pre_kernel   -scale * D_i and -LSE_i * log2(e) per query row (padded
+//   bwd_pre_kernel   -D_i and -LSE_i * log2(e) per query row (padded
 //                    to whole 128-row tiles; pad rows get D = 0, LSE = +inf so
 //                    P = 0), zeroes the fp32 dQ accumulator, and records
 //                    max |dO|, max |D| and max |V| for the scaling above. D_i = dO_i .
@@ -88,7 +88,7 @@ struct BwdArgs {
   const void *o_res;  // rounding residual of O (same 16-bit type) or null
   const float *lse;
   float *lse_l2;    // [BH, nqt*128]  -LSE * log2(e)
-  float *delta;     // [BH, nqt*128]  -scale * D
+  float *delta;     // [BH, nqt*128]  -D
   float *dq_acc;    // [BH, nqt*128, D]
   const int32_t *kv_len;
   const uint8_t *block_mask;
@@ -234,10 +234,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, long long
 #pragma unroll
     for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (live && sub == 0) {
-      // stored negated (and D pre-scaled) so the main kernel forms
-      // P = 2^(s * scale * log2 e + nl) and dS = P * (dP * scale + nd)
-      // with one packed FMA per pair
-      a.delta[row] = -a.scale * acc;
+      // stored negated so the main kernel forms P = 2^(s * scale * log2 e +
+      // nl) and dS = P * (dP * scale - scale * D) with one packed FMA per
+      // pair (the scale is applied there: the prepare phase does not take it)
+      a.delta[row] = -acc;
       amax_d = fmaxf(amax_d, fabsf(acc));
       float nl = -INFINITY;
       if (i < a.N) {
@@ -618,7 +618,8 @@ __global__ void __launch_bounds__(512, 1)
     const int key = kt * 128 + r;
     const float sl2 = a.scale_log2;
     const float f_s = exp2i(-e_s);
-    const float sc_dp = a.scale * f_s * exp2i(e_do);
+    const float sc_dp = a.scale * f_s * exp2i(e_do);  // multiplies dP16
+    const float sc_d = a.scale * f_s;                 // multiplies -D
     // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
     // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
     // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         float2 nd = nd2[4 * b];
-        fmul2(nd.x, nd.y, nd.x, nd.y, f_s, f_s);
+        fmul2(nd.x, nd.y, nd.x, nd.y, sc_d, sc_d);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll

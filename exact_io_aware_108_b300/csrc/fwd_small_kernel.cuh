@@ -30,28 +30,34 @@ template <int D>
 struct SmallCfg {
   static constexpr int kKB = D / 64;               // 128-byte column blocks
   static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile
-  static constexpr int kKStages = 1;
-  static constexpr int kVStages = 1;
+  // d = 64: P gets TMEM columns of its own and K, V get two stages each, so
+  // the next Q K^T waits only until the softmax has read S, not for P V;
+  // d = 128: P is written over S (the 256 columns hold S and O), one stage.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr int kKStages = kSepP ? 2 : 1;
+  static constexpr int kVStages = kSepP ? 2 : 1;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kBQ = 0;
-  static constexpr int kBKF = 1;
-  static constexpr int kBKE = 2;
-  static constexpr int kBVF = 3;
-  static constexpr int kBVE = 4;
-  static constexpr int kBSF = 5;   // S(t) in TMEM
-  static constexpr int kBPF = 6;   // [2] half h of P(t) in TMEM (128 arrivals)
-  static constexpr int kBOR = 8;   // P(t) V(t) done
-  static constexpr int kBDR = 9;   // drain
-  static constexpr int kNumBars = 10;
+  static constexpr int kBKF = 1;                   // [kKStages]
+  static constexpr int kBKE = kBKF + kKStages;     // [kKStages]
+  static constexpr int kBVF = kBKE + kKStages;     // [kVStages]
+  static constexpr int kBVE = kBVF + kVStages;     // [kVStages]
+  static constexpr int kBSF = kBVE + kVStages;     // S(t) in TMEM
+  static constexpr int kBSR = kBSF + 1;            // S(t) read by the softmax (128 arrivals; d = 64)
+  static constexpr int kBPF = kBSR + 1;            // [2] half h of P(t) in TMEM (128 arrivals)
+  static constexpr int kBOR = kBPF + 2;            // P(t) V(t) done
+  static constexpr int kBDR = kBOR + 1;            // drain
+  static constexpr int kNumBars = kBDR + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, list count
   static constexpr int kListOff = kMiscOff + 16;            // block-sparse: kept key tiles
   static constexpr int kMaxList = 2048;                     // nkt <= 2048
   static constexpr int kSmemBytes = kListOff + kMaxList * 2 + 1024;  // + alignment slack
-  static constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
-  static_assert(kColO + D <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kColS = 0, kColP = kSepP ? 128 : 0, kColO = kSepP ? 192 : 128;
+  static constexpr uint32_t kTmemCols = 256;
+  static_assert(kColO + D <= kTmemCols && (!kSepP || kColP + 64 <= kColO), "TMEM budget");
   // setmaxnreg split: launch with 128 registers x 256 threads (two CTAs per
   // SM); warpgroup 1 gives back to 48, the softmax warpgroup takes 208.
   static constexpr int kLaunchRegs = 128, kRegsLow = 48, kRegsHigh = 208;
@@ -90,11 +96,16 @@ __global__ void __launch_bounds__(256, 2)
 
   if (tid == 0) {
     mbar_init(bar(C::kBQ), 1);
-    mbar_init(bar(C::kBKF), 1);
-    mbar_init(bar(C::kBKE), 1);
-    mbar_init(bar(C::kBVF), 1);
-    mbar_init(bar(C::kBVE), 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(bar(C::kBKF + i), 1);
+      mbar_init(bar(C::kBKE + i), 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(bar(C::kBVF + i), 1);
+      mbar_init(bar(C::kBVE + i), 1);
+    }
     mbar_init(bar(C::kBSF), 1);
+    mbar_init(bar(C::kBSR), 128);
     mbar_init(bar(C::kBPF), 128);
     mbar_init(bar(C::kBPF + 1), 128);
     mbar_init(bar(C::kBOR), 1);
@@ -140,24 +151,29 @@ __global__ void __launch_bounds__(256, 2)
         tma_load_3d_hint(sbase + C::kQOff + kb * 16384, &tm_q, bar(C::kBQ), kb * 64, qt * 128, bh, pol_q);
       int nk = 0, nv = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        const uint32_t ph = t & 1;  // one stage each: phase = tile parity
+        const int ks = t % C::kKStages, vs = t % C::kVStages;
+        const uint32_t kph = (t / C::kKStages) & 1, vph = (t / C::kVStages) & 1;
         const int kt = SPARSE ? list[t] : t;
-        if (!mbar_wait(bar(C::kBKE), ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(C::kBKF), C::kTileBytes);
+        if (!mbar_wait(bar(C::kBKE + ks), kph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBKF + ks), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKF), kb * 64, kt * 128, kvh, pol_kv);
+          tma_load_3d_hint(sbase + C::kKOff + ks * C::kTileBytes + kb * 16384, &tm_k, bar(C::kBKF + ks),
+                           kb * 64, kt * 128, kvh, pol_kv);
         nk = t + 1;
-        if (!mbar_wait(bar(C::kBVE), ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(C::kBVF), C::kTileBytes);
+        if (!mbar_wait(bar(C::kBVE + vs), vph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(C::kBVF + vs), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
-          tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBVF), kb * 64, kt * 128, kvh, pol_kv);
+          tma_load_3d_hint(sbase + C::kVOff + vs * C::kTileBytes + kb * 16384, &tm_v, bar(C::kBVF + vs),
+                           kb * 64, kt * 128, kvh, pol_kv);
         nv = t + 1;
       }
       if (*abort_flag) {
         // let every copy still in flight land before the CTA exits
         mbar_wait_drain(bar(C::kBQ), 0, abort_flag);
-        if (nk > 0) mbar_wait_drain(bar(C::kBKF), (nk - 1) & 1, abort_flag);
-        if (nv > 0) mbar_wait_drain(bar(C::kBVF), (nv - 1) & 1, abort_flag);
+        for (int t = max(0, nk - C::kKStages); t < nk; ++t)
+          mbar_wait_drain(bar(C::kBKF + t % C::kKStages), (t / C::kKStages) & 1, abort_flag);
+        for (int t = max(0, nv - C::kVStages); t < nv; ++t)
+          mbar_wait_drain(bar(C::kBVF + t % C::kVStages), (t / C::kVStages) & 1, abort_flag);
       }
     }
   } else if (warp == 5) {
@@ -166,24 +182,49 @@ __global__ void __launch_bounds__(256, 2)
       constexpr uint32_t kIdQK = idesc_f16(BF16, 128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_f16(BF16, 128, D, false, true);
       bool ok = mbar_wait(bar(C::kBQ), 0, abort_flag);
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const uint32_t ph = t & 1;
-        if (!mbar_wait(bar(C::kBKF), ph, abort_flag)) { ok = false; break; }
-        // S holds P(t-1) until P(t-1) V(t-1) is done
-        if (t > 0 && !mbar_wait(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      // S(t) = Q K(t)^T into the S columns
+      auto issue_qk = [&](int t) {
         const uint32_t sb = opaque_u32(sbase);
+        const uint32_t kbase = sb + C::kKOff + (t % C::kKStages) * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           // A = Q, B = K_j, both K-major: 16 channels = 32 B per step
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(sb + C::kQOff + off, 16, 1024),
-                 sdesc_sw128(sb + C::kKOff + off, 16, 1024), kIdQK, k > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kColS, sdesc_sw128(sb + C::kQOff + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                 kIdQK, k > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF));
-        mma_commit(bar(C::kBKE));
-        if (!mbar_wait(bar(C::kBVF), ph, abort_flag)) { ok = false; break; }
-        const uint32_t vbase = sb + C::kVOff;
+        mma_commit(bar(C::kBKE + t % C::kKStages));
+      };
+      if constexpr (C::kSepP) {
+        // P has its own columns: S(t + 1) only waits until the softmax has
+        // read S(t), so it runs while the softmax of tile t works
+        if (ok && mbar_wait(bar(C::kBKF), 0, abort_flag)) {
+          tc_fence_after();
+          issue_qk(0);
+        } else {
+          ok = false;
+        }
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const uint32_t ph = t & 1;
+        if constexpr (C::kSepP) {
+          if (t + 1 < n_tiles) {
+            if (!mbar_wait(bar(C::kBKF + (t + 1) % C::kKStages), ((t + 1) / C::kKStages) & 1, abort_flag) ||
+                !mbar_wait(bar(C::kBSR), ph, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(t + 1);
+          }
+        } else {
+          if (!mbar_wait(bar(C::kBKF), ph, abort_flag)) { ok = false; break; }
+          // S holds P(t-1) until P(t-1) V(t-1) is done
+          if (t > 0 && !mbar_wait(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk(t);
+        }
+        const int vs = t % C::kVStages;
+        if (!mbar_wait(bar(C::kBVF + vs), (t / C::kVStages) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t vbase = opaque_u32(sbase) + C::kVOff + vs * C::kTileBytes;
         // O += P(t) V(t) in two halves of 64 keys
         for (int h = 0; h < 2; ++h) {
           if (!mbar_wait(bar(C::kBPF + h), ph, abort_flag)) { ok = false; break; }
@@ -191,11 +232,11 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
           for (int k = 4 * h; k < 4 * h + 4; ++k)
             // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
-            mma_ts(tmem + C::kColO, tmem + C::kColS + k * 8, sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdPV,
+            mma_ts(tmem + C::kColO, tmem + C::kColP + k * 8, sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdPV,
                    (t > 0 || k > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(bar(C::kBVE));
+        mma_commit(bar(C::kBVE + vs));
         mma_commit(bar(C::kBOR));
       }
       // every issued MMA must finish before TMEM is released
@@ -217,17 +258,26 @@ __global__ void __launch_bounds__(256, 2)
     const int row = tid;  // 0 .. 127
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t scol = tmem + lane_addr + C::kColS;
+    const uint32_t pcol = tmem + lane_addr + C::kColP;
     const uint32_t ocol = tmem + lane_addr + C::kColO;
     const int q_row = qt * 128 + row;
     const float sl2 = a.scale_log2;
-    // a warp whose rows all lie past N keeps only the P barriers' counts in
-    // step (S(t) complete implies their previous phase completed)
+    // a warp whose rows all lie past N keeps only the barriers' counts in
+    // step (d = 128: S(t) complete implies their previous phase completed)
     const bool pad_warp = qt * 128 + warp * 32 >= a.N;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait_warp(bar(C::kBSF), t & 1, abort_flag)) { ok = false; break; }
       if (pad_warp) {
+        if constexpr (C::kSepP) {
+          mbar_arrive(bar(C::kBSR));
+          // S(t + 1) may start before P(t) is written, so a warp without rows
+          // would run ahead into tile t + 1 and arrive on the P barriers for
+          // it while tile t's phase still waits for the other warps: it
+          // waits for P(t-1) V(t-1), which completes every earlier phase
+          if (t > 0 && !mbar_wait_warp(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
+        }
         mbar_arrive(bar(C::kBPF));
         mbar_arrive(bar(C::kBPF + 1));
         continue;
@@ -245,6 +295,10 @@ __global__ void __launch_bounds__(256, 2)
         reg_fence_32(r1);
         reg_fence_32(r2);
         reg_fence_32(r3);
+        if constexpr (C::kSepP) {  // S is in registers: the next Q K^T may overwrite it
+          tc_fence_before();
+          mbar_arrive(bar(C::kBSR));
+        }
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           s[c] = __uint_as_float(r0[c]);
@@ -259,8 +313,12 @@ __global__ void __launch_bounds__(256, 2)
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
       float m_new, alpha;
       const float nm = softmax_max(s, limit, sl2, m, m_new, alpha);
-      // S(t) complete implies P(t-1) V(t-1) is done (S(t) waited for it): O
-      // holds every earlier tile and can be rescaled
+      // O holds every earlier tile once P(t-1) V(t-1) is done (d = 128: S(t)
+      // waited for it; d = 64: wait here, which also frees the P columns)
+      if (C::kSepP && t > 0) {
+        if (!mbar_wait_warp(bar(C::kBOR), (t - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+      }
       if (t > 0 && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) {
@@ -278,7 +336,7 @@ __global__ void __launch_bounds__(256, 2)
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t hi[16];
         pack_p32<BF16>(s, c0, hi);
-        tmem_st_32x32b_x16(scol + c0 / 2, hi);
+        tmem_st_32x32b_x16(pcol + c0 / 2, hi);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -288,7 +346,7 @@ __global__ void __launch_bounds__(256, 2)
       for (int c0 = 64; c0 < 128; c0 += 32) {
         uint32_t hi[16];
         pack_p32<BF16>(s, c0, hi);
-        tmem_st_32x32b_x16(scol + c0 / 2, hi);
+        tmem_st_32x32b_x16(pcol + c0 / 2, hi);
       }
       tmem_wait_st();
       tc_fence_before();
