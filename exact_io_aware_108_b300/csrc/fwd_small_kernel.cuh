@@ -66,7 +66,7 @@ struct SmallCfg {
   static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory for two CTAs per SM");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool SPARSE = false>
+template <int D, bool BF16, bool CAUSAL, bool SPARSE = false, bool SPLIT = false>
 __global__ void __launch_bounds__(256, 2)
     fwd_small_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -137,7 +137,11 @@ __global__ void __launch_bounds__(256, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int n_tiles = SPARSE ? static_cast<int>(misc[2]) : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
+  const int n_all = SPARSE ? static_cast<int>(misc[2]) : (CAUSAL ? min(qt + 1, nkt_eff) : nkt_eff);
+  // split-KV: this CTA's contiguous share [t_lo, t_lo + n_tiles) of the tiles
+  const int split = SPLIT ? static_cast<int>(blockIdx.y) : 0;
+  int t_lo = 0, n_tiles = n_all;
+  if constexpr (SPLIT) split_share(n_all, split, a.num_splits, &t_lo, &n_tiles);
 
   if (warp >= 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(256, 2)
       for (int t = 0; t < n_tiles; ++t) {
         const int ks = t % C::kKStages, vs = t % C::kVStages;
         const uint32_t kph = (t / C::kKStages) & 1, vph = (t / C::kVStages) & 1;
-        const int kt = SPARSE ? list[t] : t;
+        const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
         if (!mbar_wait(bar(C::kBKE + ks), kph ^ 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(C::kBKF + ks), C::kTileBytes);
         for (int kb = 0; kb < C::kKB; ++kb)
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(256, 2)
         }
       }
       // mask: keys past kv_len / N, and keys after the query on the diagonal
-      const int kt = SPARSE ? list[t] : t;
+      const int kt = SPARSE ? list[t_lo + t] : t_lo + t;
       int limit = kvl - kt * 128;
       if (CAUSAL && kt == qt) limit = min(limit, row + 1);
       float m_new, alpha;
@@ -363,6 +367,10 @@ __global__ void __launch_bounds__(256, 2)
       }
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       uint16_t *orow = static_cast<uint16_t *>(a.o) + (static_cast<size_t>(bh) * a.N + q_row) * D;
+      // split-KV partial (rows < N only; the merge reads no others): O / l in
+      // fp32 and this share's LSE, in the layout fwd_merge_kernel reads
+      const size_t prow = static_cast<size_t>(split) * a.nqt * 128 * (gridDim.x / a.nqt) +
+                          static_cast<size_t>(bh) * a.nqt * 128 + static_cast<size_t>(q_row);
 #pragma unroll 1
       for (int j = 0; j < D / 32; ++j) {
         uint32_t o[32];
@@ -373,6 +381,16 @@ __global__ void __launch_bounds__(256, 2)
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if constexpr (SPLIT) {
+          if (q_row < a.N) {
+            float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * D + 32 * j);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              dst[i / 4] = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                       __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+          }
+          continue;
         }
         uint32_t pk[16], rk[16];
 #pragma unroll
@@ -394,7 +412,7 @@ __global__ void __launch_bounds__(256, 2)
         }
       }
       if (q_row < a.N)
-        a.lse[static_cast<size_t>(bh) * a.N + q_row] =
+        (SPLIT ? a.lse_part[prow] : a.lse[static_cast<size_t>(bh) * a.N + q_row]) =
             (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
     // teardown of the softmax warpgroup

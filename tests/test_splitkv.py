@@ -59,13 +59,15 @@ def test_splitkv_matches_oracle(B, H, Hkv, N, d, dt, causal, S):
     check("LSE", lse.cpu(), lse_ref, TOL_LSE, torch.float32)
 
 
-def test_splitkv_key_padding_down_to_no_keys():
+@pytest.mark.parametrize("d,dt", [(128, "bf16"), (64, "bf16")])
+def test_splitkv_key_padding_down_to_no_keys(d, dt):
     """kv_len 0 (every share empty: O = 0, LSE = -inf), 1, a tile boundary
-    and a ragged length; sharp softmax."""
-    t = inputs.make_qkv(4, 2, 700, 128, "bf16", seed=5, qk_mult=2.0, with_dout=False)
+    and a ragged length; sharp softmax. d = 64 runs the shares two CTAs per
+    SM, d = 128 one."""
+    t = inputs.make_qkv(4, 2, 700, d, dt, seed=5, qk_mult=2.0, with_dout=False)
     kv_len = torch.tensor([0, 1, 256, 613], dtype=torch.int32)
     q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(d)
     o, lse = _splitkv(q, k, v, scale, False, 4, kv_len=kv_len.cuda())
     o_ref, lse_ref = ref.attn_fwd(t["q"], t["k"], t["v"], scale, False, kv_len)
     check("O", o.cpu(), o_ref, TOL_O, q.dtype)
