@@ -103,6 +103,9 @@ struct BwdArgs {
   unsigned int *stats;
   const void *v;     // V, read by bwd_pre_kernel for max |V|
   long long n_v16;   // 16-byte chunks of V
+  const void *k;      // K, prefetched into L2 one work item ahead
+  unsigned int *work;  // work-item counter of the main kernel, zeroed before its launch
+  int n_items;         // work items: B * Hkv * nkt
   int H, N, nqt, nkt;
   int hgroup;    // heads per scheduling group (causal launch order, see below)
   int Hkv;       // key/value heads (grouped-query attention: H = Hkv * kv_group)
@@ -314,18 +317,25 @@ struct BwdCfg {
   static constexpr int kLseOff = kdSOff + 32768;           // 2 stages x 128 fp32
   static constexpr int kDeltaOff = kLseOff + 1024;         // 2 stages x 128 fp32
   static constexpr int kBarOff = kDeltaOff + 1024;
-  static constexpr int kBKV = 0, kBQF = 1, kBQE = 3, kBSF = 5, kBDPF = 6, kBPR = 7 /* x2 */,
-                       kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13, kBDSF = 14,
-                       kBCK = 15 /* K ready in fp16, 384 arrivals */,
-                       kBCV = 16 /* V ready in fp16, 384 arrivals */,
-                       kNumBars = 17;
+  // Barriers. Per query tile (phase = the CTA's running tile count): Q/dO
+  // stage full/empty, S^T, dP^T, P^T halves, dV issued, dS^T, dQ full/empty,
+  // dS^T read. Per work item (phase = the CTA's running count of items with
+  // work): K landed, V landed, K and V in fp16 (256 arrivals), all products
+  // done, dK/dV read out of TMEM (256 arrivals). Item slots: full (the
+  // producer) and empty (13 consumer arrivals: the MMA thread and the warps
+  // of the three compute warpgroups). kBEND: the MMA thread's final drain.
+  static constexpr int kBKL = 0, kBQF = 1 /* x2 */, kBQE = 3 /* x2 */, kBSF = 5, kBDPF = 6,
+                       kBPR = 7 /* x2 */, kBDV = 9, kBDSR = 10, kBDQF = 11, kBDQE = 12, kBFIN = 13,
+                       kBDSF = 14, kBCK = 15, kBCV = 16, kBVL = 17, kBACC = 18, kBITF = 19 /* x2 */,
+                       kBITE = 21 /* x2 */, kBEND = 23, kNumBars = 24;
+  static constexpr int kItemConsumers = 1 + 12;
   // d = 128: the dQ partial is computed transposed (dQ^T = K^T dS^T, TMEM
   // lane = head-dim channel, column = query) so one warp's reduction into
   // the fp32 accumulator covers 32 consecutive channels of a row: a whole
   // 128-byte line per instruction instead of 32 scattered 16-byte pieces.
   static constexpr bool kDqT = (D == 128);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // misc: [0] TMEM address, [1] abort flag
+  // misc: [0] TMEM address, [1] abort flag, [2..3] work item slots
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr uint32_t kColDQ = kDqT ? kColDP : 2 * D + 256;
@@ -349,6 +359,53 @@ __device__ __forceinline__ int next_kept(const uint8_t *mask, int nkt, int nqt, 
   return i;
 }
 
+// Work item of the backward: one key tile of one key/value head, and the
+// (query head, query tile) pairs of its group that see it.
+struct BwdItem {
+  int bkv;      // [B*Hkv] key/value head
+  int kt;       // key tile
+  int kvl;      // keys of this batch entry (kv_len clamped to [0, N])
+  int n_iter;   // (query head, query tile) pairs walked
+  int q_first;  // first query tile walked for each query head
+};
+
+template <bool CAUSAL, bool SPARSE>
+__device__ __forceinline__ BwdItem bwd_item(const BwdArgs &a, int w) {
+  const WorkItem wi = grouped_item(w, a.n_items / a.nkt, a.nkt, a.hgroup, false);
+  BwdItem it;
+  it.bkv = wi.bh;
+  it.kt = wi.tile;
+  int kvl = a.N;
+  if (a.kv_len != nullptr) {
+    const int v = a.kv_len[it.bkv / a.Hkv];
+    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
+  }
+  it.kvl = kvl;
+  // query tiles that see this key tile: [q_begin, nqt), filtered by the mask
+  const int q_begin = CAUSAL ? it.kt : 0;
+  int n = 0;
+  if (it.kt * 128 < kvl) {
+    if (SPARSE) {
+      for (int i = 0; i < a.nqt; ++i) n += a.block_mask[static_cast<size_t>(i) * a.nkt + it.kt] != 0;
+    } else {
+      n = a.nqt - q_begin;
+    }
+  }
+  // grouped-query attention: every query head of the group, (g, qi) in order
+  it.n_iter = n * a.kv_group;
+  it.q_first = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, it.kt, 0) : q_begin;
+  return it;
+}
+
+// Persistent backward: one CTA per SM takes work items (key tile, key/value
+// head) from a counter, in the grouped order of grouped_item: groups of
+// hgroup heads, key tile major inside a group, so the heaviest items
+// (causal: low key tiles see the most query tiles) start first while the
+// heads that run concurrently stay few enough for their Q and dO to stay in
+// L2. Between two items the next item's V and K loads start as soon as the
+// last dP^T and dQ products of the previous item have read them, and the
+// dK/dV epilogue and the last dQ reductions of the previous item overlap
+// the next item's start.
 template <int D, bool BF16, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -364,52 +421,38 @@ __global__ void __launch_bounds__(512, 1)
   }
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
   volatile uint32_t *abort_flag = misc + 1;
+  volatile int *item_slot = reinterpret_cast<volatile int *>(misc + 2);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
-
-  // Launch order: groups of hgroup heads; within a group key tile major,
-  // so the heaviest CTAs of the group (causal: low key tiles see the most
-  // query tiles) start first, while the heads that run concurrently stay
-  // few enough for their Q and dO to stay in L2.
-  // key/value head ([B*Hkv] index) and key tile of this CTA
-  const WorkItem item =
-      grouped_item(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x) / a.nkt, a.nkt, a.hgroup, false);
-  const int bkv = item.bh, kt = item.tile;
-  const int b = bkv / a.Hkv;
-  int kvl = a.N;
-  if (a.kv_len != nullptr) {
-    const int v = a.kv_len[b];
-    kvl = v < 0 ? 0 : (v > a.N ? a.N : v);
-  }
-  // query tiles that see this key tile: [q_begin, nqt), filtered by the mask
-  const bool key_tile_live = kt * 128 < kvl;
-  const int q_begin = CAUSAL ? kt : 0;
-  int n_iter = 0;
-  if (key_tile_live) {
-    if (SPARSE) {
-      for (int i = 0; i < a.nqt; ++i) n_iter += a.block_mask[static_cast<size_t>(i) * a.nkt + kt] != 0;
-    } else {
-      n_iter = a.nqt - q_begin;
-    }
-  }
-  // grouped-query attention: the CTA walks every query head of its group,
-  // (g, qi) in order, accumulating their dK and dV in TMEM
-  n_iter *= a.kv_group;
-  const int q_first = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, 0) : q_begin;
-  auto advance = [&](int &g, int &qi) {
-    qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, kt, qi + 1) : qi + 1;
+  auto advance = [&](const BwdItem &it, int &g, int &qi) {
+    qi = SPARSE ? next_kept(a.block_mask, a.nkt, a.nqt, it.kt, qi + 1) : qi + 1;
     if (qi >= a.nqt) {
       ++g;
-      qi = q_first;
+      qi = it.q_first;
     }
+  };
+  // consumer side of the item slots: item k of this CTA (-1: no more work);
+  // one arrival per consumer warp (the MMA thread arrives alone)
+  auto take_item = [&](int k, bool whole_warp, int &w) -> bool {
+    const int s = k & 1;
+    const bool got = whole_warp ? mbar_wait_warp(bar(C::kBITF + s), (k >> 1) & 1, abort_flag)
+                                : mbar_wait(bar(C::kBITF + s), (k >> 1) & 1, abort_flag);
+    if (!got) return false;
+    w = item_slot[s];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(bar(C::kBITE + s));
+    return true;
   };
 
   if (blockIdx.x == 0 && tid == 0) a.stats[3] = static_cast<unsigned int>(ds_exponent(a.stats, a.scale, D));
   if (tid == 0) {
-    mbar_init(bar(C::kBKV), 1);
+    mbar_init(bar(C::kBKL), 1);
+    mbar_init(bar(C::kBVL), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kBQF + s), 1);
       mbar_init(bar(C::kBQE + s), 1);
       mbar_init(bar(C::kBPR + s), 128);
+      mbar_init(bar(C::kBITF + s), 1);
+      mbar_init(bar(C::kBITE + s), C::kItemConsumers);
     }
     mbar_init(bar(C::kBSF), 1);
     mbar_init(bar(C::kBDPF), 1);
@@ -419,8 +462,10 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(C::kBDQE), 128);
     mbar_init(bar(C::kBFIN), 1);
     mbar_init(bar(C::kBDSF), 1);
-    mbar_init(bar(C::kBCK), 384);
-    mbar_init(bar(C::kBCV), 384);
+    mbar_init(bar(C::kBCK), 256);
+    mbar_init(bar(C::kBCV), 256);
+    mbar_init(bar(C::kBACC), 256);
+    mbar_init(bar(C::kBEND), 1);
     *abort_flag = 0u;
     fence_barrier_init();
     prefetch_tensormap(&tm_q);
@@ -442,41 +487,82 @@ __global__ void __launch_bounds__(512, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0 && !pipelines_starved()) {
+    if (lane == 0) {
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      mbar_arrive_expect_tx(bar(C::kBKV), 2 * C::kTileBytes);
-      for (int kb = 0; kb < C::kKB; ++kb) {
-        tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKV), kb * 64, kt * 128, bkv, pol_kv);
-        tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBKV), kb * 64, kt * 128, bkv, pol_kv);
-      }
-      int g = 0, qi = q_first;
-      int issued = 0;
-      for (int u = 0; u < n_iter; ++u) {
-        const int st = u & 1;
-        if (!mbar_wait(bar(C::kBQE + st), ((u >> 1) & 1) ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(C::kBQF + st), 2 * C::kTileBytes + 1024);
-        for (int kb = 0; kb < C::kKB; ++kb) {
-          tma_load_3d_hint(sbase + C::kQOff + st * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQF + st),
-                           kb * 64, qi * 128, a.q_head(bkv, g), pol_q);
-          tma_load_3d_hint(sbase + C::kdOOff + st * C::kTileBytes + kb * 16384, &tm_do,
-                           bar(C::kBQF + st), kb * 64, qi * 128, a.q_head(bkv, g), pol_q);
+      int U = 0;                        // Q/dO tiles issued
+      int u_last = -1;                  // last tile of the previous item with work
+      int k_issued = 0, v_issued = 0;   // K and V loads issued
+      bool ok = true;
+      int w = static_cast<int>(blockIdx.x);  // the grid never exceeds the item count
+      item_slot[0] = w;
+      mbar_arrive(bar(C::kBITF));
+      for (int k = 0; w >= 0; ++k) {
+        if (pipelines_starved()) break;  // test switch: issue nothing, every wait runs out
+        const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
+        int g = 0, qi = it.q_first;
+        for (int u = 0; u < it.n_iter; ++u) {
+          const int st = U & 1;
+          if (!mbar_wait(bar(C::kBQE + st), ((U >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(C::kBQF + st), 2 * C::kTileBytes + 1024);
+          const int qh = a.q_head(it.bkv, g);
+          for (int kb = 0; kb < C::kKB; ++kb) {
+            tma_load_3d_hint(sbase + C::kQOff + st * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQF + st),
+                             kb * 64, qi * 128, qh, pol_q);
+            tma_load_3d_hint(sbase + C::kdOOff + st * C::kTileBytes + kb * 16384, &tm_do,
+                             bar(C::kBQF + st), kb * 64, qi * 128, qh, pol_q);
+          }
+          const long long r0 = qh * tile_rows + static_cast<long long>(qi) * 128;
+          bulk_load(sbase + C::kLseOff + st * 512, a.lse_l2 + r0, 512, bar(C::kBQF + st));
+          bulk_load(sbase + C::kDeltaOff + st * 512, a.delta + r0, 512, bar(C::kBQF + st));
+          ++U;
+          advance(it, g, qi);
+          if (u == 0) {
+            // this item's V once the previous item's last dP^T product has
+            // read V, its K once the last dQ product has read K
+            if (u_last >= 0 && !mbar_wait(bar(C::kBDPF), u_last & 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(C::kBVL), C::kTileBytes);
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d_hint(sbase + C::kVOff + kb * 16384, &tm_v, bar(C::kBVL), kb * 64, it.kt * 128, it.bkv,
+                               pol_kv);
+            ++v_issued;
+            if (u_last >= 0 && !mbar_wait(bar(C::kBDQF), u_last & 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(C::kBKL), C::kTileBytes);
+            for (int kb = 0; kb < C::kKB; ++kb)
+              tma_load_3d_hint(sbase + C::kKOff + kb * 16384, &tm_k, bar(C::kBKL), kb * 64, it.kt * 128, it.bkv,
+                               pol_kv);
+            ++k_issued;
+          }
         }
-        const long long r0 = a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128;
-        bulk_load(sbase + C::kLseOff + st * 512, a.lse_l2 + r0, 512, bar(C::kBQF + st));
-        bulk_load(sbase + C::kDeltaOff + st * 512, a.delta + r0, 512, bar(C::kBQF + st));
-        issued = u + 1;
-        advance(g, qi);
+        if (!ok) break;
+        if (it.n_iter > 0) u_last = U - 1;
+        // the next item goes to the other slot once every consumer has read
+        // the item before it; its K and V are pulled into L2 meanwhile
+        const int s1 = (k + 1) & 1;
+        if (k >= 1 && !mbar_wait(bar(C::kBITE + s1), (((k + 1) >> 1) - 1) & 1, abort_flag)) break;
+        int w1 = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(a.work, 1u));
+        if (w1 >= a.n_items) w1 = -1;
+        item_slot[s1] = w1;
+        mbar_arrive(bar(C::kBITF + s1));
+        if (w1 >= 0) {
+          const WorkItem nx = grouped_item(w1, a.n_items / a.nkt, a.nkt, a.hgroup, false);
+          const uint32_t bytes = static_cast<uint32_t>(min(128, a.N - nx.tile * 128)) * D * 2;
+          const size_t off = (static_cast<size_t>(nx.bh) * a.N + static_cast<size_t>(nx.tile) * 128) * D * 2;
+          bulk_prefetch_l2(static_cast<const uint8_t *>(a.k) + off, bytes);
+          bulk_prefetch_l2(static_cast<const uint8_t *>(a.v) + off, bytes);
+        }
+        w = w1;
       }
       if (*abort_flag) {
-        mbar_wait_drain(bar(C::kBKV), 0, abort_flag);
-        for (int u = max(0, issued - 2); u < issued; ++u)
-          mbar_wait_drain(bar(C::kBQF + (u & 1)), (u >> 1) & 1, abort_flag);
+        // let the copies in flight land before the CTA exits
+        if (k_issued > 0) mbar_wait_drain(bar(C::kBKL), (k_issued - 1) & 1, abort_flag);
+        if (v_issued > 0) mbar_wait_drain(bar(C::kBVL), (v_issued - 1) & 1, abort_flag);
+        for (int t = max(0, U - 2); t < U; ++t) mbar_wait_drain(bar(C::kBQF + (t & 1)), (t >> 1) & 1, abort_flag);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0) {
       // every operand is fp16 (bf16 inputs are converted; see the top)
       constexpr uint32_t kIdSS = idesc_f16(false, 128, 128, false, false);   // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(false, 128, D, false, true);      // dK, dV
@@ -494,86 +580,107 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(bar(C::kBSF));
       };
-      // K and V landed, and (bf16 inputs) K converted
-      bool ok = mbar_wait(bar(C::kBKV), 0, abort_flag) && mbar_wait(bar(C::kBCK), 0, abort_flag) &&
-                mbar_wait(bar(C::kBQF), 0, abort_flag);
-      if (ok) {
+      int U = 0;   // query tiles processed
+      int kl = 0;  // items with work processed
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int w;
+        if (!take_item(k, false, w) || w < 0) break;
+        const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
+        if (it.n_iter == 0) continue;
+        // K landed (and, bf16 inputs, converted), the first Q stage landed,
+        // and the previous tile's dV products are done reading P^T from the
+        // S^T columns
+        ok = mbar_wait(bar(C::kBKL), kl & 1, abort_flag) && mbar_wait(bar(C::kBCK), kl & 1, abort_flag) &&
+             mbar_wait(bar(C::kBQF + (U & 1)), (U >> 1) & 1, abort_flag) &&
+             (U == 0 || mbar_wait(bar(C::kBDV), (U - 1) & 1, abort_flag));
+        if (!ok) break;
         tc_fence_after();
-        issue_s(0);
-      }
-      for (int u = 0; ok && u < n_iter; ++u) {
-        const int st = u & 1;
-        const uint32_t sb = opaque_u32(sbase);
-        const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff, sDS = sb + C::kdSOff;
-        const uint32_t sQ = sb + C::kQOff + st * C::kTileBytes;
-        const uint32_t sdO = sb + C::kdOOff + st * C::kTileBytes;
-        // d = 128: the dP^T columns hold the previous dQ partial until read out
-        if (C::kDqT && u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
-        // the first dP^T needs V in fp16
-        if (u == 0 && !mbar_wait(bar(C::kBCV), 0, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
-                 kIdSS, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBDPF));
-        // dV_j += P^T dO_i, P^T read from TMEM, one 64-query half at a time
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!mbar_wait(bar(C::kBPR + h), u & 1, abort_flag)) { ok = false; break; }
+        issue_s(U & 1);
+        for (int u = 0; u < it.n_iter; ++u, ++U) {
+          const int st = U & 1;
+          const uint32_t sb = opaque_u32(sbase);
+          const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff, sDS = sb + C::kdSOff;
+          const uint32_t sQ = sb + C::kQOff + st * C::kTileBytes;
+          const uint32_t sdO = sb + C::kdOOff + st * C::kTileBytes;
+          // d = 128: the dP^T columns hold the previous dQ partial until read out
+          if (C::kDqT && U > 0 && !mbar_wait(bar(C::kBDQE), (U - 1) & 1, abort_flag)) { ok = false; break; }
+          // the first dP^T of an item needs its V (in fp16)
+          if (u == 0 && !(mbar_wait(bar(C::kBVL), kl & 1, abort_flag) && mbar_wait(bar(C::kBCV), kl & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks,
-                   sdesc_sw128(sdO + (4 * h + ks) * 2048, 16384, 1024), kIdKV,
-                   (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
+                   kIdSS, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBDPF));
+          // the first dV product of an item overwrites the accumulators: the
+          // previous item's dK and dV must have been read out of TMEM
+          if (u == 0 && kl > 0 && !mbar_wait(bar(C::kBACC), (kl - 1) & 1, abort_flag)) { ok = false; break; }
+          // dV_j += P^T dO_i, P^T read from TMEM, one 64-query half at a time
+          for (int h = 0; ok && h < 2; ++h) {
+            if (!mbar_wait(bar(C::kBPR + h), U & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks,
+                     sdesc_sw128(sdO + (4 * h + ks) * 2048, 16384, 1024), kIdKV,
+                     (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          mma_commit(bar(C::kBDV));
+          if (C::kSAfterDV && u + 1 < it.n_iter) {
+            // next score tile: its Q stage must have landed, and the S^T
+            // columns are free once this tile's dV products have read P^T
+            if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((U + 1) >> 1) & 1, abort_flag) ||
+                !mbar_wait(bar(C::kBDV), U & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(st ^ 1);
+          }
+          if (!mbar_wait(bar(C::kBDSR), U & 1, abort_flag)) { ok = false; break; }
+          // d = 64: the dQ columns hold the previous partial until read out
+          if (!C::kDqT && U > 0 && !mbar_wait(bar(C::kBDQE), (U - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // dQ first, so its read-out overlaps the next S^T and the dK MMA
+          if constexpr (C::kDqT) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + ks * 2048, 16384, 1024),
+                     sdesc_sw128(sDS + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)  // dQ_i = dS K_j (dS read MN-major from the dS^T buffer)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
+                     sdesc_sw128(sK + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBDQF));
+          if (!C::kSAfterDV && u + 1 < it.n_iter) {
+            // next score tile: its Q stage must have landed, and the S^T
+            // columns are free once this tile's dV products have read P^T
+            if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((U + 1) >> 1) & 1, abort_flag) ||
+                !mbar_wait(bar(C::kBDV), U & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(st ^ 1);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
+            mma_ss(tmem + C::kColDK,
+                   sdesc_sw128(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                   sdesc_sw128(sQ + ks * 2048, 16384, 1024), kIdKV, (u > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(C::kBDSF));
+          mma_commit(bar(C::kBQE + st));
         }
         if (!ok) break;
-        mma_commit(bar(C::kBDV));
-        if (C::kSAfterDV && u + 1 < n_iter) {
-          // next score tile: its Q stage must have landed, and the S^T
-          // columns are free once this tile's dV products have read P^T
-          if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((u + 1) >> 1) & 1, abort_flag) ||
-              !mbar_wait(bar(C::kBDV), u & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(st ^ 1);
-        }
-        if (!mbar_wait(bar(C::kBDSR), u & 1, abort_flag)) { ok = false; break; }
-        // d = 64: the dQ columns hold the previous partial until read out
-        if (!C::kDqT && u > 0 && !mbar_wait(bar(C::kBDQE), (u - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // dQ first, so its read-out overlaps the next S^T and the dK MMA
-        if constexpr (C::kDqT) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + ks * 2048, 16384, 1024),
-                   sdesc_sw128(sDS + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQ_i = dS K_j (dS read MN-major from the dS^T buffer)
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
-                   sdesc_sw128(sK + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBDQF));
-        if (!C::kSAfterDV && u + 1 < n_iter) {
-          // next score tile: its Q stage must have landed, and the S^T
-          // columns are free once this tile's dV products have read P^T
-          if (!mbar_wait(bar(C::kBQF + (st ^ 1)), ((u + 1) >> 1) & 1, abort_flag) ||
-              !mbar_wait(bar(C::kBDV), u & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(st ^ 1);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
-          mma_ss(tmem + C::kColDK,
-                 sdesc_sw128(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(sQ + ks * 2048, 16384, 1024), kIdKV, (u > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(C::kBDSF));
-        mma_commit(bar(C::kBQE + st));
+        mma_commit(bar(C::kBFIN));
+        ++kl;
       }
-      mma_commit(bar(C::kBFIN));
-      mbar_wait_drain(bar(C::kBFIN), 0, abort_flag);
+      // every issued product completes before TMEM is released
+      mma_commit(bar(C::kBEND));
+      mbar_wait_drain(bar(C::kBEND), 0, abort_flag);
     }
   }
     // teardown of warpgroup 0 (the two register regions do not rejoin)
@@ -587,39 +694,18 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // ---- prologue of warpgroups 1-3 (bf16 inputs): K_j, then V_j -> fp16
-    // in place. The first S^T needs only K; the first dP^T waits for V.
-    if (n_iter > 0) {
-      constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
-      float amax = 0.f;
-      const bool landed = BF16 && mbar_wait_warp(bar(C::kBKV), 0, abort_flag);
-      if (landed) {
-        uint4 *kt16 = reinterpret_cast<uint4 *>(smem + C::kKOff);
-        for (int c = tid - 128; c < kChunks; c += 384) kt16[c] = bf16x8_to_f16x8(kt16[c], amax);
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBCK));
-      if (landed) {
-        uint4 *vt16 = reinterpret_cast<uint4 *>(smem + C::kVOff);
-        for (int c = tid - 128; c < kChunks; c += 384) vt16[c] = bf16x8_to_f16x8(vt16[c], amax);
-        if (amax > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBCV));
-    }
     const int e_s = ds_exponent(a.stats, a.scale, D);
     const int e_do = BF16 ? do_exponent(a.stats) : 0;
     if (warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T, one query half
     const int h = (warp >> 2) - 1;  // query half: columns [64h, 64h+64) of the tile
     const int r = tid & 127;         // key row of this thread's lane (epilogue)
-    const int key = kt * 128 + r;
     const float sl2 = a.scale_log2;
     const float f_s = exp2i(-e_s);
     const float sc_dp = a.scale * f_s * exp2i(e_do);  // multiplies dP16
     const float sc_d = a.scale * f_s;                 // multiplies -D
+    // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO)
+    const float f_out = exp2i(h == 0 ? e_s : e_do);
     // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
     // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
     // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
@@ -629,194 +715,233 @@ __global__ void __launch_bounds__(512, 1)
     const int t4 = lane >> 2, c4 = lane & 3;
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const uint32_t sDS = sbase + C::kdSOff + h * 16384;
-    bool ok = true;
-    int g = 0, qi = q_first;
-    for (int u = 0; u < n_iter; ++u) {
-      const int st = u & 1;
-      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + C::kLseOff + st * 512 + h * 256) + c4;
-      const float2 *nd2 = reinterpret_cast<const float2 *>(smem + C::kDeltaOff + st * 512 + h * 256) + c4;
-      if (!mbar_wait_warp(bar(C::kBQF + st), (u >> 1) & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(C::kBSF), u & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      // p[j][4b + 2i + e]: key (j, i), query 8b + 2c4 + e of this half, fp32,
-      // kept in registers for dS
-      float p[2][32];
-      {
-        uint32_t sv[2][32];
-        tmem_ld_16x256b_x8(tq + C::kColS + 64 * h, sv[0]);
-        tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColS + 64 * h, sv[1]);
-        tmem_wait_ld();
-        reg_fence_32(sv[0]);
-        reg_fence_32(sv[1]);
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const float2 nl = nl2[4 * b];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int e = 4 * b + 2 * i;
-              ffma2(p[j][e], p[j][e + 1], __uint_as_float(sv[j][e]), __uint_as_float(sv[j][e + 1]), sl2,
-                    sl2, nl.x, nl.y);
-              p[j][e] = ex2_approx(p[j][e]);
-              p[j][e + 1] = ex2_approx(p[j][e + 1]);
-            }
+    int U = 0, kl = 0;
+    for (int k = 0;; ++k) {
+      int w;
+      if (!take_item(k, true, w) || w < 0) break;
+      const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
+      const int kt = it.kt, kvl = it.kvl;
+      bool ok = true, have = false;
+      if (it.n_iter > 0) {
+        // ---- bf16 inputs: K_j, then V_j -> fp16 in place. The first S^T
+        // needs only K; the first dP^T waits for V.
+        constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
+        float amax = 0.f;
+        const bool k_in = !BF16 || mbar_wait_warp(bar(C::kBKL), kl & 1, abort_flag);
+        if (BF16 && k_in) {
+          uint4 *k16 = reinterpret_cast<uint4 *>(smem + C::kKOff);
+          for (int c = tid - 128; c < kChunks; c += 256) k16[c] = bf16x8_to_f16x8(k16[c], amax);
+          fence_proxy_async_smem();
         }
-        // causal: query c of this tile sees key k iff qi*128 + c >= kt*128 + k;
-        // a dead key sees nothing. Local column 8b + 2c4 + e is query
-        // 64h + 8b + 2c4 + e of the tile.
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int kk = kt * 128 + 32 * (warp & 3) + 16 * j + 8 * i + t4;
-            const int cmin = (kk >= kvl ? 128 : (CAUSAL ? (kk - qi * 128) : -1)) - 64 * h;
-            if (cmin > 0) {
-#pragma unroll
-              for (int b = 0; b < 8; ++b)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                  if (8 * b + 2 * c4 + e < cmin) p[j][4 * b + 2 * i + e] = 0.f;
-            }
-          }
-      }
-      // P^T (16-bit pairs, column = query pair) into the first 32 columns of
-      // this half's S^T columns (already read)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t w[16];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          w[2 * b] = pack2<false>(p[j][4 * b], p[j][4 * b + 1]);
-          w[2 * b + 1] = pack2<false>(p[j][4 * b + 2], p[j][4 * b + 3]);
+        tc_fence_before();
+        mbar_arrive(bar(C::kBCK));
+        const bool v_in = k_in && (!BF16 || mbar_wait_warp(bar(C::kBVL), kl & 1, abort_flag));
+        if (BF16 && v_in) {
+          uint4 *v16 = reinterpret_cast<uint4 *>(smem + C::kVOff);
+          for (int c = tid - 128; c < kChunks; c += 256) v16[c] = bf16x8_to_f16x8(v16[c], amax);
+          if (amax > 65504.f) atomicOr(&g_fa_device_error, kDevErrRange);
+          fence_proxy_async_smem();
         }
-        tmem_st_16x128b_x8(tq + (static_cast<uint32_t>(16 * j) << 16) + C::kColS + 64 * h, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBPR + h));
-      if (!mbar_wait_warp(bar(C::kBDPF), u & 1, abort_flag)) { ok = false; break; }
-      // the previous dQ/dK MMAs must be done reading dS before it is rewritten
-      if (u > 0 && !mbar_wait_warp(bar(C::kBDSF), (u - 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t dv[2][32];
-      tmem_ld_16x256b_x8(tq + C::kColDP + 64 * h, dv[0]);
-      tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColDP + 64 * h, dv[1]);
-      tmem_wait_ld();
-      reg_fence_32(dv[0]);
-      reg_fence_32(dv[1]);
+        tc_fence_before();
+        mbar_arrive(bar(C::kBCV));
+        ok = v_in;
+        int g = 0, qi = it.q_first;
+        for (const int u_end = U + it.n_iter; ok && U < u_end; ++U) {
+          const int st = U & 1;
+          const float2 *nl2 = reinterpret_cast<const float2 *>(smem + C::kLseOff + st * 512 + h * 256) + c4;
+          const float2 *nd2 = reinterpret_cast<const float2 *>(smem + C::kDeltaOff + st * 512 + h * 256) + c4;
+          if (!mbar_wait_warp(bar(C::kBQF + st), (U >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(bar(C::kBSF), U & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // p[j][4b + 2i + e]: key (j, i), query 8b + 2c4 + e of this half, fp32,
+          // kept in registers for dS
+          float p[2][32];
+          {
+            uint32_t sv[2][32];
+            tmem_ld_16x256b_x8(tq + C::kColS + 64 * h, sv[0]);
+            tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColS + 64 * h, sv[1]);
+            tmem_wait_ld();
+            reg_fence_32(sv[0]);
+            reg_fence_32(sv[1]);
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        float2 nd = nd2[4 * b];
-        fmul2(nd.x, nd.y, nd.x, nd.y, sc_d, sc_d);
+            for (int b = 0; b < 8; ++b) {
+              const float2 nl = nl2[4 * b];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+              for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            // dS * scale * 2^-e_s = P * (dP16 * scale * 2^(e_do - e_s) - scale * D * 2^-e_s)
-            const int e = 4 * b + 2 * i;
-            float t0, t1;
-            ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), sc_dp, sc_dp, nd.x,
-                  nd.y);
-            fmul2(t0, t1, t0, t1, p[j][e], p[j][e + 1]);
-            // row = key of the dS^T tile; queries 8b + 2c4, +1 are the 4-byte
-            // word c4 of 16-byte chunk b of the row's 128 bytes in region h,
-            // swizzled by (row & 7) = t4
-            const int row = 32 * (warp & 3) + 16 * j + 8 * i + t4;
-            const uint32_t addr = sDS + row * 128 + ((b ^ t4) << 4) + 4 * c4;
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<false>(t0, t1)) : "memory");
+                for (int i = 0; i < 2; ++i) {
+                  const int e = 4 * b + 2 * i;
+                  ffma2(p[j][e], p[j][e + 1], __uint_as_float(sv[j][e]), __uint_as_float(sv[j][e + 1]), sl2,
+                        sl2, nl.x, nl.y);
+                  p[j][e] = ex2_approx(p[j][e]);
+                  p[j][e + 1] = ex2_approx(p[j][e + 1]);
+                }
+            }
+            // causal: query c of this tile sees key k iff qi*128 + c >= kt*128 + k;
+            // a dead key sees nothing. Local column 8b + 2c4 + e is query
+            // 64h + 8b + 2c4 + e of the tile.
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const int kk = kt * 128 + 32 * (warp & 3) + 16 * j + 8 * i + t4;
+                const int cmin = (kk >= kvl ? 128 : (CAUSAL ? (kk - qi * 128) : -1)) - 64 * h;
+                if (cmin > 0) {
+#pragma unroll
+                  for (int b = 0; b < 8; ++b)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                      if (8 * b + 2 * c4 + e < cmin) p[j][4 * b + 2 * i + e] = 0.f;
+                }
+              }
           }
+          // P^T (16-bit pairs, column = query pair) into the first 32 columns of
+          // this half's S^T columns (already read)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint32_t pw[16];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+              pw[2 * b] = pack2<false>(p[j][4 * b], p[j][4 * b + 1]);
+              pw[2 * b + 1] = pack2<false>(p[j][4 * b + 2], p[j][4 * b + 3]);
+            }
+            tmem_st_16x128b_x8(tq + (static_cast<uint32_t>(16 * j) << 16) + C::kColS + 64 * h, pw);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBPR + h));
+          if (!mbar_wait_warp(bar(C::kBDPF), U & 1, abort_flag)) { ok = false; break; }
+          // the previous dQ/dK MMAs must be done reading dS before it is rewritten
+          if (U > 0 && !mbar_wait_warp(bar(C::kBDSF), (U - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t dv[2][32];
+          tmem_ld_16x256b_x8(tq + C::kColDP + 64 * h, dv[0]);
+          tmem_ld_16x256b_x8(tq + (16u << 16) + C::kColDP + 64 * h, dv[1]);
+          tmem_wait_ld();
+          reg_fence_32(dv[0]);
+          reg_fence_32(dv[1]);
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            float2 nd = nd2[4 * b];
+            fmul2(nd.x, nd.y, nd.x, nd.y, sc_d, sc_d);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                // dS * scale * 2^-e_s = P * (dP16 * scale * 2^(e_do - e_s) - scale * D * 2^-e_s)
+                const int e = 4 * b + 2 * i;
+                float t0, t1;
+                ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), sc_dp, sc_dp, nd.x,
+                      nd.y);
+                fmul2(t0, t1, t0, t1, p[j][e], p[j][e + 1]);
+                // row = key of the dS^T tile; queries 8b + 2c4, +1 are the 4-byte
+                // word c4 of 16-byte chunk b of the row's 128 bytes in region h,
+                // swizzled by (row & 7) = t4
+                const int row = 32 * (warp & 3) + 16 * j + 8 * i + t4;
+                const uint32_t addr = sDS + row * 128 + ((b ^ t4) << 4) + 4 * c4;
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<false>(t0, t1)) : "memory");
+              }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBDSR));
+          advance(it, g, qi);
+        }
+        have = ok && mbar_wait_warp(bar(C::kBFIN), kl & 1, abort_flag);
+        if (have) tc_fence_after();
+        ++kl;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBDSR));
-      advance(g, qi);
-    }
-    // ---- epilogue: warpgroup 1 writes dK, warpgroup 2 writes dV
-    bool have = ok && n_iter > 0;
-    if (have) {
-      have = mbar_wait_warp(bar(C::kBFIN), 0, abort_flag);
-      tc_fence_after();
-    }
-    uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
-                    (static_cast<size_t>(bkv) * a.N + static_cast<size_t>(key)) * D;
-    uint32_t v[D / 32][32];
-    if (have) {
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j)
-        tmem_ld_32x32b_x32(tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV) + 32 * j, v[j]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) reg_fence_32(v[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[j][i] = 0u;
-    }
-    if (key < a.N) {
-      // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO)
-      const float u = exp2i(h == 0 ? e_s : e_do);
-#pragma unroll
+      // ---- dK (warpgroup 1) or dV (warpgroup 2), 32 channels at a time out
+      // of TMEM (zeros for an item without work or after a stop); the next
+      // item's first dV product waits until both are read
+      const int key = kt * 128 + r;
+      uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
+                      (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(key)) * D;
+#pragma unroll 1
       for (int j = 0; j < D / 32; ++j) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
-        float f[32];
+        uint32_t v[32];
+        if (have) {
+          tmem_ld_32x32b_x32(tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV) + 32 * j, v);
+          tmem_wait_ld();
+          reg_fence_32(v);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) fmul2(f[i], f[i + 1], __uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]), u, u);
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (key < a.N) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
+          float x[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack2<BF16>(f[8 * q], f[8 * q + 1]), pack2<BF16>(f[8 * q + 2], f[8 * q + 3]),
-                             pack2<BF16>(f[8 * q + 4], f[8 * q + 5]), pack2<BF16>(f[8 * q + 6], f[8 * q + 7]));
+          for (int i = 0; i < 32; i += 2)
+            fmul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), f_out, f_out);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack2<BF16>(x[8 * q], x[8 * q + 1]), pack2<BF16>(x[8 * q + 2], x[8 * q + 3]),
+                               pack2<BF16>(x[8 * q + 4], x[8 * q + 5]), pack2<BF16>(x[8 * q + 6], x[8 * q + 7]));
+        }
       }
+      if (have) {
+        tc_fence_before();
+        mbar_arrive(bar(C::kBACC));
+      }
+      if (!ok) break;
     }
     } else {
     // ------------------------------------------------------------ dQ partials
     const int r = tid & 127;  // d = 128: head-dim channel; d = 64: query row
-    int g = 0, qi = q_first;
-    for (int u = 0; u < n_iter; ++u) {
-      if (!mbar_wait_warp(bar(C::kBDQF), u & 1, abort_flag)) break;
-      tc_fence_after();
-      // read the whole partial into registers, release the TMEM columns
-      // (the next dP^T or dQ MMA may overwrite them), then reduce into the
-      // accumulator
-      constexpr int kCols = C::kDqT ? 128 : D;
-      uint32_t v[kCols / 32][32];
+    int U = 0;
+    for (int k = 0;; ++k) {
+      int w;
+      if (!take_item(k, true, w) || w < 0) break;
+      const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
+      bool ok = true;
+      int g = 0, qi = it.q_first;
+      for (int u = 0; u < it.n_iter; ++u, ++U) {
+        if (!mbar_wait_warp(bar(C::kBDQF), U & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // read the whole partial into registers, release the TMEM columns
+        // (the next dP^T or dQ MMA may overwrite them), then reduce into the
+        // accumulator
+        constexpr int kCols = C::kDqT ? 128 : D;
+        uint32_t v[kCols / 32][32];
 #pragma unroll
-      for (int j = 0; j < kCols / 32; ++j) tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDQ + j * 32, v[j]);
-      tmem_wait_ld();
+        for (int j = 0; j < kCols / 32; ++j) tmem_ld_32x32b_x32(tmem + lane_addr + C::kColDQ + j * 32, v[j]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < kCols / 32; ++j) reg_fence_32(v[j]);
-      tc_fence_before();
-      mbar_arrive(bar(C::kBDQE));
-      if constexpr (C::kDqT) {
-        // thread r holds channel r of the 128 queries of this tile. The L2
-        // takes the reductions more slowly than the warps issue them; a short
-        // pause after every 16 keeps the sub-partition's memory-instruction
-        // queue from filling, so the softmax warpgroups' shared-memory
-        // accesses behind it are not held up (measured 4-5 % faster).
-        float *acc = a.dq_acc + (a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128) * D + r;
+        for (int j = 0; j < kCols / 32; ++j) reg_fence_32(v[j]);
+        tc_fence_before();
+        mbar_arrive(bar(C::kBDQE));
+        if constexpr (C::kDqT) {
+          // thread r holds channel r of the 128 queries of this tile. The L2
+          // takes the reductions more slowly than the warps issue them; a short
+          // pause after every 16 keeps the sub-partition's memory-instruction
+          // queue from filling, so the softmax warpgroups' shared-memory
+          // accesses behind it are not held up (measured 4-5 % faster).
+          float *acc = a.dq_acc + (a.q_head(it.bkv, g) * tile_rows + static_cast<long long>(qi) * 128) * D + r;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]));
-            if ((i & 15) == 15) {
-              const long long t0 = clock64();
-              while (clock64() - t0 < 120) {
+            for (int i = 0; i < 32; ++i) {
+              atomicAdd(acc + (j * 32 + i) * D, __uint_as_float(v[j][i]));
+              if ((i & 15) == 15) {
+                const long long t0 = clock64();
+                while (clock64() - t0 < 120) {
+                }
               }
             }
-          }
-      } else {
-        float *acc = a.dq_acc + (a.q_head(bkv, g) * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
+        } else {
+          float *acc = a.dq_acc + (a.q_head(it.bkv, g) * tile_rows + static_cast<long long>(qi) * 128 + r) * D;
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j)
+          for (int j = 0; j < D / 32; ++j)
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            atomicAdd(reinterpret_cast<float4 *>(acc + j * 32 + i),
-                      make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
-                                  __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
+            for (int i = 0; i < 32; i += 4)
+              atomicAdd(reinterpret_cast<float4 *>(acc + j * 32 + i),
+                        make_float4(__uint_as_float(v[j][i]), __uint_as_float(v[j][i + 1]),
+                                    __uint_as_float(v[j][i + 2]), __uint_as_float(v[j][i + 3])));
+        }
+        advance(it, g, qi);
       }
-      advance(g, qi);
+      if (!ok) break;
     }
     }
     // teardown of the compute warpgroups

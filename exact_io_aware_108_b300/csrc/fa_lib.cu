@@ -555,6 +555,9 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     }
   }
   if (phases & kMain) {
+    // the persistent main kernel takes its work items from this counter
+    e = cudaMemsetAsync(a.work, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd work counter reset");
     fa_status r;
     if (sparse)
       r = launch_bwd_main_t<D, BF16, false, true>(tq, tk, tv, tdo, a, grid, st);
@@ -650,12 +653,9 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.dq_acc = reinterpret_cast<float *>(ws + 2 * up256(rows * 4));
   a.kv_len = kv_len;
   a.block_mask = block_mask;
-  a.q = q;
-  a.q16 = q16;
-  a.do16 = do16;
-  a.stats = stats;
-  a.v = v;
-  a.n_v16 = BHkv * static_cast<long long>(N) * d / 8;
+  a.k = k;
+  a.work = stats + 8;
+  a.n_items = static_cast<int>(BHkv * s.nqt);
   a.H = H;
   a.N = N;
   a.nqt = s.nqt;
@@ -668,7 +668,8 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.scale_log2 = scale * 1.4426950408889634f;
   const long long rows_pad = static_cast<long long>(rows);
   const long long n_vec4 = s.BH * static_cast<long long>(N) * d / 4;
-  const int grid = static_cast<int>(BHkv * s.nqt);  // one CTA per (batch, key/value head, key tile)
+  // persistent: one CTA per SM (at most one per work item)
+  const int grid = static_cast<int>(std::min<long long>(BHkv * s.nqt, sm_count()));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
   if (d == 64)

@@ -266,7 +266,8 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int causal, int
  * sizes. With R = B * H * ceil(N / 128) * 128 query rows padded to whole
  * tiles: fp32 LSE * log2(e) [R], fp32 D = rowsum(dO * O) [R] and an fp32 dQ
  * accumulator [R, d], each rounded up to 256 bytes; 256 bytes of statistics
- * (max |dO|, max |D|, max |V|, the dS exponent); then room for fp16 copies of Q and of the scaled dO
+ * (max |dO|, max |D|, max |V|, the dS exponent, the main kernel's work-item
+ * counter); then room for fp16 copies of Q and of the scaled dO
  * ([B, H, N, d] each, rounded up to 256 bytes; used for bf16 inputs only).
  * Returns 0 for invalid sizes.
  */
