@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "bd59ba930fce69399d71c208d6afcf067a9a2bc6806abf11d0ec91f701f452a1",
-    "bytes_per_launch": {"4096": 4 * (203650048 + 85442048), "8192": 4 * (249488640 + 117703168),
-                         "16384": 4 * (250043648 + 122826752)},
+    "source_sha256": "4ff23059086d39efb4819a42e4c77cc15cf4bb644d51de4126e8b248568144a3",
+    "bytes_per_launch": {"4096": 4 * (204180224 + 84145152), "8192": 4 * (249728768 + 117001472),
+                         "16384": 4 * (250371584 + 120447232)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
