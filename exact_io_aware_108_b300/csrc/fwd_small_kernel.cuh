@@ -390,24 +390,24 @@ __global__ void __launch_bounds__(256, 2)
               dst[i / 4] = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
                                        __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
           }
-          continue;
-        }
-        uint32_t pk[16], rk[16];
+        } else {
+          uint32_t pk[16], rk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
-          pk[i] = pack2<BF16>(x0, x1);
-          rk[i] = pack2<BF16>(x0 - unpack_lo<BF16>(pk[i]), x1 - unpack_hi<BF16>(pk[i]));
-        }
-        if (q_row < a.N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = __uint_as_float(o[2 * i]) * inv_l, x1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+            pk[i] = pack2<BF16>(x0, x1);
+            rk[i] = pack2<BF16>(x0 - unpack_lo<BF16>(pk[i]), x1 - unpack_hi<BF16>(pk[i]));
+          }
+          if (q_row < a.N) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * j);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          if (a.o_res != nullptr) {
-            uint4 *dr = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.o_res) +
-                                                  (orow - static_cast<uint16_t *>(a.o)) + 32 * j);
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if (a.o_res != nullptr) {
+              uint4 *dr = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.o_res) +
+                                                    (orow - static_cast<uint16_t *>(a.o)) + 32 * j);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dr[v] = make_uint4(rk[4 * v], rk[4 * v + 1], rk[4 * v + 2], rk[4 * v + 3]);
+              for (int v = 0; v < 4; ++v) dr[v] = make_uint4(rk[4 * v], rk[4 * v + 1], rk[4 * v + 2], rk[4 * v + 3]);
+            }
           }
         }
       }
