@@ -432,10 +432,12 @@ __global__ void __launch_bounds__(512, 1)
   };
   // consumer side of the item slots: item k of this CTA (-1: no more work);
   // one arrival per consumer warp (the MMA thread arrives alone)
+  // (after a stop the roles keep taking items: the compute warpgroups write
+  // zeros for them)
   auto take_item = [&](int k, bool whole_warp, int &w) -> bool {
     const int s = k & 1;
-    const bool got = whole_warp ? mbar_wait_warp(bar(C::kBITF + s), (k >> 1) & 1, abort_flag)
-                                : mbar_wait(bar(C::kBITF + s), (k >> 1) & 1, abort_flag);
+    bool got = mbar_wait_handoff(bar(C::kBITF + s), (k >> 1) & 1, abort_flag);
+    if (whole_warp) got = __all_sync(0xffffffffu, got);
     if (!got) return false;
     w = item_slot[s];
     if (whole_warp) __syncwarp();
@@ -498,10 +500,12 @@ __global__ void __launch_bounds__(512, 1)
       item_slot[0] = w;
       mbar_arrive(bar(C::kBITF));
       for (int k = 0; w >= 0; ++k) {
-        if (pipelines_starved()) break;  // test switch: issue nothing, every wait runs out
+        // after a stop, or with the test switch (every wait then runs out),
+        // the items are handed on without loads
         const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
+        ok = !*abort_flag && !pipelines_starved();
         int g = 0, qi = it.q_first;
-        for (int u = 0; u < it.n_iter; ++u) {
+        for (int u = 0; ok && u < it.n_iter; ++u) {
           const int st = U & 1;
           if (!mbar_wait(bar(C::kBQE + st), ((U >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(C::kBQF + st), 2 * C::kTileBytes + 1024);
@@ -534,17 +538,16 @@ __global__ void __launch_bounds__(512, 1)
             ++k_issued;
           }
         }
-        if (!ok) break;
-        if (it.n_iter > 0) u_last = U - 1;
+        if (ok && it.n_iter > 0) u_last = U - 1;
         // the next item goes to the other slot once every consumer has read
         // the item before it; its K and V are pulled into L2 meanwhile
         const int s1 = (k + 1) & 1;
-        if (k >= 1 && !mbar_wait(bar(C::kBITE + s1), (((k + 1) >> 1) - 1) & 1, abort_flag)) break;
+        if (k >= 1 && !mbar_wait_handoff(bar(C::kBITE + s1), (((k + 1) >> 1) - 1) & 1, abort_flag)) break;
         int w1 = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(a.work, 1u));
         if (w1 >= a.n_items) w1 = -1;
         item_slot[s1] = w1;
         mbar_arrive(bar(C::kBITF + s1));
-        if (w1 >= 0) {
+        if (w1 >= 0 && !*abort_flag) {
           const WorkItem nx = grouped_item(w1, a.n_items / a.nkt, a.nkt, a.hgroup, false);
           const uint32_t bytes = static_cast<uint32_t>(min(128, a.N - nx.tile * 128)) * D * 2;
           const size_t off = (static_cast<size_t>(nx.bh) * a.N + static_cast<size_t>(nx.tile) * 128) * D * 2;
@@ -582,19 +585,20 @@ __global__ void __launch_bounds__(512, 1)
       };
       int U = 0;   // query tiles processed
       int kl = 0;  // items with work processed
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
+      for (int k = 0;; ++k) {
         int w;
         if (!take_item(k, false, w) || w < 0) break;
+        if (*abort_flag) continue;
         const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
         if (it.n_iter == 0) continue;
+        bool ok;
         // K landed (and, bf16 inputs, converted), the first Q stage landed,
         // and the previous tile's dV products are done reading P^T from the
         // S^T columns
         ok = mbar_wait(bar(C::kBKL), kl & 1, abort_flag) && mbar_wait(bar(C::kBCK), kl & 1, abort_flag) &&
              mbar_wait(bar(C::kBQF + (U & 1)), (U >> 1) & 1, abort_flag) &&
              (U == 0 || mbar_wait(bar(C::kBDV), (U - 1) & 1, abort_flag));
-        if (!ok) break;
+        if (!ok) continue;
         tc_fence_after();
         issue_s(U & 1);
         for (int u = 0; u < it.n_iter; ++u, ++U) {
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(bar(C::kBDSF));
           mma_commit(bar(C::kBQE + st));
         }
-        if (!ok) break;
+        if (!ok) continue;
         mma_commit(bar(C::kBFIN));
         ++kl;
       }
@@ -721,8 +725,8 @@ __global__ void __launch_bounds__(512, 1)
       if (!take_item(k, true, w) || w < 0) break;
       const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
       const int kt = it.kt, kvl = it.kvl;
-      bool ok = true, have = false;
-      if (it.n_iter > 0) {
+      bool ok = !*abort_flag, have = false;
+      if (ok && it.n_iter > 0) {
         // ---- bf16 inputs: K_j, then V_j -> fp16 in place. The first S^T
         // needs only K; the first dP^T waits for V.
         constexpr int kChunks = C::kTileBytes / 16;  // 16-byte chunks per tile
@@ -884,7 +888,6 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(bar(C::kBACC));
       }
-      if (!ok) break;
     }
     } else {
     // ------------------------------------------------------------ dQ partials
@@ -893,11 +896,11 @@ __global__ void __launch_bounds__(512, 1)
     for (int k = 0;; ++k) {
       int w;
       if (!take_item(k, true, w) || w < 0) break;
+      if (*abort_flag) continue;
       const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
-      bool ok = true;
       int g = 0, qi = it.q_first;
       for (int u = 0; u < it.n_iter; ++u, ++U) {
-        if (!mbar_wait_warp(bar(C::kBDQF), U & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(C::kBDQF), U & 1, abort_flag)) break;
         tc_fence_after();
         // read the whole partial into registers, release the TMEM columns
         // (the next dP^T or dQ MMA may overwrite them), then reduce into the
@@ -941,7 +944,6 @@ __global__ void __launch_bounds__(512, 1)
         }
         advance(it, g, qi);
       }
-      if (!ok) break;
     }
     }
     // teardown of the compute warpgroups

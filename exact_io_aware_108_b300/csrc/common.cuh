@@ -71,6 +71,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Wait for a work-item hand-over between the roles of a persistent kernel:
+// bounded like a drain (it ignores the abort flag), so that after a stop the
+// roles still walk the remaining items together (writing zeros for them);
+// false only when the hand-over itself ran out of time.
+__device__ __forceinline__ bool mbar_wait_handoff(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, false);
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity,
                                                 volatile uint32_t *abort_flag) {

@@ -58,9 +58,12 @@ def test_forward_wait_runs_out_then_recovers(B, H, N, d, causal):
         check("LSE", lse[b, h, rows].cpu(), lse_ref, TOL_LSE, torch.float32)
 
 
-def test_backward_wait_runs_out_then_recovers():
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 2, 384, 128),    # fewer key tiles than SMs: one work item per CTA
+    (2, 8, 2048, 128),   # more key tiles than SMs: CTAs keep taking items after the stop
+])
+def test_backward_wait_runs_out_then_recovers(B, H, N, d):
     import exact_io_aware_108_b300 as fa
-    B, H, N, d = 1, 2, 384, 128
     t = inputs.make_qkv(B, H, N, d, "bf16", seed=42, qk_mult=2.0)
     q, k, v, do = (x.cuda() for x in (t["q"], t["k"], t["v"], t["dout"]))
     scale = 1.0 / math.sqrt(d)
@@ -71,6 +74,9 @@ def test_backward_wait_runs_out_then_recovers():
     assert torch.all(dk == 0) and torch.all(dv == 0)
     dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, scale, causal=True, o_res=res)
     assert fa.fa_get_device_error() == 0
+    if N > 512:  # the recovery is checked against the oracle on the small case
+        assert torch.isfinite(dk).all() and torch.isfinite(dv).all() and bool((dk != 0).any())
+        return
     g = ref.attn_bwd(t["q"], t["k"], t["v"], t["dout"], scale, True, rows_per_task=64)
     check("dQ", dq.cpu(), g[0], TOL_GRAD, q.dtype)
     check("dK", dk.cpu(), g[1], TOL_GRAD, q.dtype)
