@@ -708,8 +708,6 @@ __global__ void __launch_bounds__(512, 1)
     const float f_s = exp2i(-e_s);
     const float sc_dp = a.scale * f_s * exp2i(e_do);  // multiplies dP16
     const float sc_d = a.scale * f_s;                 // multiplies -D
-    // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO)
-    const float f_out = exp2i(h == 0 ? e_s : e_do);
     // TMEM is read and written in 16-lane blocks j = 0, 1 of the warp's
     // quadrant (16x256b loads, 16x128b stores): in block j this thread holds
     // lanes t4 and t4 + 8, i.e. the keys 32 (warp & 3) + 16 j + 8 i + t4
@@ -861,6 +859,9 @@ __global__ void __launch_bounds__(512, 1)
       const int key = kt * 128 + r;
       uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
                       (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(key)) * D;
+      // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO); read again
+      // here rather than kept in a register through the tile loop
+      const float f_out = exp2i(h == 0 ? ds_exponent(a.stats, a.scale, D) : (BF16 ? do_exponent(a.stats) : 0));
 #pragma unroll 1
       for (int j = 0; j < D / 32; ++j) {
         uint32_t v[32];
