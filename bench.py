@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "4ff23059086d39efb4819a42e4c77cc15cf4bb644d51de4126e8b248568144a3",
-    "bytes_per_launch": {"4096": 4 * (204180224 + 84145152), "8192": 4 * (249728768 + 117001472),
-                         "16384": 4 * (250371584 + 120447232)},
+    "source_sha256": "5b0d324a2af776a977fadcc485da1463eb7aa3f0fd074622c0b716e2f961b76b",
+    "bytes_per_launch": {"4096": 4 * (203988480 + 83645952), "8192": 4 * (248982784 + 115856128),
+                         "16384": 4 * (248417024 + 119564800)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
