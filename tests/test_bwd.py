@@ -115,6 +115,37 @@ def test_bwd_dk_dv_deterministic():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
+@pytest.mark.parametrize("B,H,Hkv,N,d,dt,causal,sparse", [
+    (4, 8, 8, 1100, 128, "bf16", True, False),   # 288 key tiles, ragged tail
+    (2, 16, 4, 1536, 64, "f16", False, False),   # grouped heads: 96 items of 4 query heads each
+    (1, 8, 8, 2560, 64, "bf16", False, True),    # block-sparse, 30 % of the tiles kept
+])
+def test_bwd_persistent_items_repeatable(B, H, Hkv, N, d, dt, causal, sparse):
+    """The main kernel runs one CTA per SM that takes work items (key tile,
+    key/value head) from a counter; with many more items than SMs, repeated
+    calls must give bitwise the same dK and dV (each key tile is summed in
+    one CTA in a fixed order, whichever CTA takes it), and dQ within the
+    rounding of its unordered fp32 reductions."""
+    import exact_io_aware_108_b300 as fa
+    t = inputs.make_qkv(B, H, N, d, dt, seed=23, hkv=Hkv)
+    q, k, v, do = (t[n].cuda() for n in ("q", "k", "v", "dout"))
+    bm = inputs.make_block_mask(N, 0.3, seed=5).to(torch.uint8).cuda() if sparse else None
+    scale = 1.0 / math.sqrt(d)
+    o, lse, o_res = fa.attention_forward(q, k, v, scale, causal=causal, block_mask=bm, return_residual=True)
+    first = None
+    for _ in range(8):
+        dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, scale, causal=causal, block_mask=bm,
+                                           o_res=o_res)
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_error() == 0
+        if first is None:
+            first = (dq.clone(), dk.clone(), dv.clone())
+            assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+            continue
+        assert torch.equal(dk, first[1]) and torch.equal(dv, first[2])
+        assert (dq.float() - first[0].float()).abs().max().item() <= 2.0 ** -6 * first[0].float().abs().max().item()
+
+
 # ----------------------------------------------------- full-size workloads
 
 FULL_SIZE = [
