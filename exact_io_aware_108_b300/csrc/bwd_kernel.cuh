@@ -822,6 +822,11 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld();
           reg_fence_32(dv[0]);
           reg_fence_32(dv[1]);
+          // ds[j][i][b]: key (j, i), queries 8b + 2c4, +1 of this half, as a
+          // 16-bit pair; for fixed (j, i, b) the warp holds one 8 x 8 block of
+          // dS^T (rows = 8 keys, columns = 8 queries) in the m8n8 fragment
+          // layout (row lane / 4, column pair lane % 4)
+          uint32_t ds[2][2][8];
 #pragma unroll
           for (int b = 0; b < 8; ++b) {
             float2 nd = nd2[4 * b];
@@ -836,14 +841,23 @@ __global__ void __launch_bounds__(512, 1)
                 ffma2(t0, t1, __uint_as_float(dv[j][e]), __uint_as_float(dv[j][e + 1]), sc_dp, sc_dp, nd.x,
                       nd.y);
                 fmul2(t0, t1, t0, t1, p[j][e], p[j][e + 1]);
-                // row = key of the dS^T tile; queries 8b + 2c4, +1 are the 4-byte
-                // word c4 of 16-byte chunk b of the row's 128 bytes in region h,
-                // swizzled by (row & 7) = t4
-                const int row = 32 * (warp & 3) + 16 * j + 8 * i + t4;
-                const uint32_t addr = sDS + row * 128 + ((b ^ t4) << 4) + 4 * c4;
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack2<false>(t0, t1)) : "memory");
+                ds[j][i][b] = pack2<false>(t0, t1);
               }
           }
+          // four blocks per stmatrix: blocks b = 4q .. 4q + 3 of key rows
+          // 32 (warp & 3) + 16 j + 8 i + 0..7; lane l gives the address of
+          // row l % 8 of block l / 8: 16-byte chunk b of the row's 128 bytes
+          // in region h, swizzled by (row & 7)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int rr = lane & 7, bb = 4 * q + (lane >> 3);
+                const uint32_t addr = sDS + (32 * (warp & 3) + 16 * j + 8 * i + rr) * 128 + ((bb ^ rr) << 4);
+                stmatrix_x4(addr, ds[j][i][4 * q], ds[j][i][4 * q + 1], ds[j][i][4 * q + 2], ds[j][i][4 * q + 3]);
+              }
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(bar(C::kBDSR));

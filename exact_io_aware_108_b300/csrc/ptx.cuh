@@ -53,6 +53,15 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Four 8 x 8 blocks of 16-bit values to shared memory: lane l holds
+// elements (l / 4, 2 (l % 4) .. +1) of block k in r_k, and gives the address
+// of row l % 8 of block l / 8 (16 contiguous bytes).
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // Bulk prefetch of [src, src + bytes) from global memory into L2 (no
 // completion to wait for). src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
