@@ -40,9 +40,10 @@
 //                    by up to ~0.05 at d = 128, which reaches dQ and dK.
 //   bwd_cvt_kernel   (bf16 inputs) Q -> fp16 and dO -> fp16 * 2^-e_do into
 //                    the workspace, read by the main kernel's tensor maps.
-//   bwd_main_kernel  one CTA per 128-key tile of one (batch, key/value head);
-//                    K_j, V_j stay in shared memory (converted there to fp16
-//                    for bf16 inputs), dK_j and dV_j stay in TMEM, and the
+//   bwd_main_kernel  persistent, one CTA per SM; its work items are the
+//                    128-key tiles j of each (batch, key/value head). Per
+//                    item K_j, V_j stay in shared memory (converted there to
+//                    fp16 for bf16 inputs), dK_j and dV_j stay in TMEM, and the
 //                    CTA loops over the query tiles that see key tile j, of
 //                    every query head that reads this key/value head (one
 //                    head unless the attention is grouped-query).
@@ -52,17 +53,20 @@
 //
 // Main-kernel roles (512 threads; setmaxnreg moves registers from
 // warpgroup 0 to the other three):
-//   warp 0 lane 0   TMA: K_j, V_j once; Q_i, dO_i tiles and the LSE/D rows of
-//                   query tile i through a two-stage ring.
+//   warp 0 lane 0   work items (from the counter, handed to the other roles
+//                   through two shared-memory slots); TMA: K_j, V_j once per
+//                   item; Q_i, dO_i tiles and the LSE/D rows of query tile i
+//                   through a two-stage ring.
 //   warp 1          TMEM allocation; lane 0 issues every tcgen05.mma.
-//   warpgroups 1-3  at the start: K_j, V_j -> fp16 in place (bf16 inputs).
+//   warpgroups 1, 2 at the start of an item: K_j, V_j -> fp16 in place (bf16
+//                   inputs).
 //   warpgroups 1, 2 one 64-query half h of the tile each: P^T -> TMEM
 //                   (fp16), dS^T -> shared memory (fp16, scale and 2^-e_s
 //                   folded in, computed from the fp32 P). A thread holds 4
 //                   keys x 16 queries (16-lane TMEM shapes), so it reads only
 //                   16 of the half's per-query LSE and D values; at the end
-//                   warpgroup 1 writes dK, warpgroup 2 writes dV (one key
-//                   row per thread).
+//                   of an item warpgroup 1 writes dK, warpgroup 2 writes dV
+//                   (one key row per thread).
 //   warpgroup 3     reads the dQ partial from TMEM and adds it to the fp32
 //                   accumulator (d = 128: thread r owns head-dim
 //                   channel r of the transposed partial; d = 64: thread r
