@@ -325,8 +325,12 @@ fa_status fa_bwd_blocksparse(const void *q, const void *k, const void *v, const 
  *                   records max |dO|, max |D| and max |V|; for bf16 inputs
  *                   writes the fp16 copies of Q and of the scaled dO into the
  *                   workspace.
- *   fa_bwd_main     one CTA per 128-key tile: dK and dV (written directly),
- *                   dQ partials added into the accumulator. block_mask NULL
+ *   fa_bwd_main     zeroes the work-item counter in the workspace (a 4-byte
+ *                   memset on the stream), then one persistent kernel (one
+ *                   CTA per SM) takes the 128-key tiles of each key/value
+ *                   head from it: dK and dV (written directly), dQ partials
+ *                   added into the accumulator. Two fa_bwd_main calls that
+ *                   share a workspace must not overlap. block_mask NULL
  *                   means dense/causal (causal applies only then); kv_len
  *                   must be NULL when block_mask is given
  *                   (FA_ERR_INVALID_ARG otherwise).
