@@ -575,15 +575,26 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t kIdKV = idesc_f16(false, 128, D, false, true);      // dK, dV
       constexpr uint32_t kIdQ = C::kDqT ? idesc_f16(false, 128, 128, true, true)  // dQ^T
                                         : idesc_f16(false, 128, D, true, true);   // dQ
+      // Shared-memory descriptors as 32-bit low words (the high word, SBO =
+      // 1024 and the 128-byte swizzle, is the same for all): K-major tiles
+      // (LBO 16) and MN-major tiles (LBO 16384, the distance between
+      // 64-column blocks); a step of off bytes adds off / 16. Kept few and
+      // cheap: this thread shares its sub-partition with three busy warps,
+      // and every instruction it issues delays the next product.
+      // (The words are derived per tile from an opaque copy of the shared
+      // base, so the compiler does not hoist every step out of the loops
+      // into this thread's few registers.)
+      constexpr uint32_t kHi = sdesc_hi(1024);
+      constexpr uint32_t kStageStep = C::kTileBytes >> 4;
       // S^T = K_j Q_i^T for the query tile in stage st
       auto issue_s = [&](int st) {
         const uint32_t sb = opaque_u32(sbase);
-        const uint32_t sK = sb + C::kKOff, sQ = sb + C::kQOff + st * C::kTileBytes;
+        const uint32_t k_k = sdesc_lo(sb + C::kKOff, 16);
+        const uint32_t q_k = sdesc_lo(sb + C::kQOff, 16) + st * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
-                 kIdSS, ks > 0 ? 1u : 0u);
+          const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          mma_ss_w(tmem + C::kColS, k_k + o, q_k + o, kHi, kIdSS, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF));
       };
@@ -608,9 +619,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = 0; u < it.n_iter; ++u, ++U) {
           const int st = U & 1;
           const uint32_t sb = opaque_u32(sbase);
-          const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff, sDS = sb + C::kdSOff;
-          const uint32_t sQ = sb + C::kQOff + st * C::kTileBytes;
-          const uint32_t sdO = sb + C::kdOOff + st * C::kTileBytes;
+          const uint32_t do_k = sdesc_lo(sb + C::kdOOff, 16) + st * kStageStep;
           // d = 128: the dP^T columns hold the previous dQ partial until read out
           if (C::kDqT && U > 0 && !mbar_wait(bar(C::kBDQE), (U - 1) & 1, abort_flag)) { ok = false; break; }
           // the first dP^T of an item needs its V (in fp16)
@@ -621,9 +630,8 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {  // dP^T = V_j dO_i^T
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
-                   kIdSS, ks > 0 ? 1u : 0u);
+            const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            mma_ss_w(tmem + C::kColDP, sdesc_lo(sb + C::kVOff, 16) + o, do_k + o, kHi, kIdSS, ks > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kBDPF));
           // the first dV product of an item overwrites the accumulators: the
@@ -633,11 +641,11 @@ __global__ void __launch_bounds__(512, 1)
           for (int h = 0; ok && h < 2; ++h) {
             if (!mbar_wait(bar(C::kBPR + h), U & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
+            const uint32_t do_mn = sdesc_lo(opaque_u32(sbase) + C::kdOOff, 16384) + st * kStageStep;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              mma_ts(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks,
-                     sdesc_sw128(sdO + (4 * h + ks) * 2048, 16384, 1024), kIdKV,
-                     (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
+              mma_ts_w(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks, do_mn + (4 * h + ks) * 128, kHi,
+                       kIdKV, (u > 0 || h > 0 || ks > 0) ? 1u : 0u);
           }
           if (!ok) break;
           mma_commit(bar(C::kBDV));
@@ -654,16 +662,16 @@ __global__ void __launch_bounds__(512, 1)
           if (!C::kDqT && U > 0 && !mbar_wait(bar(C::kBDQE), (U - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           // dQ first, so its read-out overlaps the next S^T and the dK MMA
+          const uint32_t sb2 = opaque_u32(sbase);
+          const uint32_t k_mn = sdesc_lo(sb2 + C::kKOff, 16384), ds_mn = sdesc_lo(sb2 + C::kdSOff, 16384);
           if constexpr (C::kDqT) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + ks * 2048, 16384, 1024),
-                     sdesc_sw128(sDS + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+              mma_ss_w(tmem + C::kColDQ, k_mn + ks * 128, ds_mn + ks * 128, kHi, kIdQ, ks > 0 ? 1u : 0u);
           } else {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // dQ_i = dS K_j (dS read MN-major from the dS^T buffer)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, 16384, 1024),
-                     sdesc_sw128(sK + ks * 2048, 16384, 1024), kIdQ, ks > 0 ? 1u : 0u);
+              mma_ss_w(tmem + C::kColDQ, ds_mn + ks * 128, k_mn + ks * 128, kHi, kIdQ, ks > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kBDQF));
           if (!C::kSAfterDV && u + 1 < it.n_iter) {
@@ -674,11 +682,13 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             issue_s(st ^ 1);
           }
+          const uint32_t sb3 = opaque_u32(sbase);
+          const uint32_t ds_k = sdesc_lo(sb3 + C::kdSOff, 16);
+          const uint32_t q_mn = sdesc_lo(sb3 + C::kQOff, 16384) + st * kStageStep;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
-            mma_ss(tmem + C::kColDK,
-                   sdesc_sw128(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                   sdesc_sw128(sQ + ks * 2048, 16384, 1024), kIdKV, (u > 0 || ks > 0) ? 1u : 0u);
+            mma_ss_w(tmem + C::kColDK, ds_k + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), q_mn + ks * 128, kHi,
+                     kIdKV, (u > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar(C::kBDSF));
           mma_commit(bar(C::kBQE + st));
         }
