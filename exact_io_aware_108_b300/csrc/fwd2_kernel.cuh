@@ -205,16 +205,19 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t qbase = sb + C::kQOff + x * C::kTileBytes;
         if constexpr (FP8) {
           // 32 e4m3 elements = 32 B of the single 128-byte column block per step
+          const uint32_t q_k = sdesc_lo(qbase, 16), k_k = sdesc_lo(kbase, 16);
 #pragma unroll
           for (int ks = 0; ks < D / 32; ++ks)
-            mma_ss_f8(tmem + C::col_s(x), sdesc_sw128(qbase + ks * 32, 16, 1024),
-                      sdesc_sw128(kbase + ks * 32, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+            mma_ss_f8_w(tmem + C::col_s(x), q_k + ks * 2, k_k + ks * 2, sdesc_hi(1024), kIdQK, ks > 0 ? 1u : 0u);
         } else {
+          // descriptors as 32-bit words stepped by adds (sdesc_lo): this
+          // thread shares its sub-partition with the softmax warps, and
+          // every instruction it issues delays the next product
+          const uint32_t q_k = sdesc_lo(qbase, 16), k_k = sdesc_lo(kbase, 16);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::col_s(x), sdesc_sw128(qbase + off, 16, 1024),
-                   sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+            const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            mma_ss_w(tmem + C::col_s(x), q_k + o, k_k + o, sdesc_hi(1024), kIdQK, ks > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar(C::kBSF + x));
@@ -250,15 +253,15 @@ __global__ void __launch_bounds__(384, 1)
             if constexpr (FP8) {
               // A = P (4 keys per TMEM column, 8 columns per step); B = V^T
               // K-major, 32 keys = 32 B per step
+              const uint32_t v_k = sdesc_lo(vbase, 16);
 #pragma unroll
               for (int ks = 2 * h; ks < 2 * h + 2; ++ks)
-                mma_ts_f8(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 32, 16, 1024), kIdPV,
-                          (t > 0 || ks > 0) ? 1u : 0u);
+                mma_ts_f8_w(ocol, pcol + ks * 8, v_k + ks * 2, sdesc_hi(1024), kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
             } else {
+              const uint32_t v_mn = sdesc_lo(vbase, 16384);
 #pragma unroll
               for (int ks = 4 * h; ks < 4 * h + 4; ++ks)
-                mma_ts(ocol, pcol + ks * 8, sdesc_sw128(vbase + ks * 2048, 16384, 1024), kIdPV,
-                       (t > 0 || ks > 0) ? 1u : 0u);
+                mma_ts_w(ocol, pcol + ks * 8, v_mn + ks * 128, sdesc_hi(1024), kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
             }
           }
           if (!ok) break;

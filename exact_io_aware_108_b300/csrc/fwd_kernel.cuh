@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int ks = 4 * h; ks < 4 * h + 4; ++ks) {
               // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
-              const uint64_t bd = sdesc_sw128(vbase + ks * 2048, 16384, 1024);
-              mma_ts(tmem + C::kColO, pcol + ks * 8, bd, kIdPV, (u > 0 || ks > 0) ? 1u : 0u);
+              mma_ts_w(tmem + C::kColO, pcol + ks * 8, sdesc_lo(vbase, 16384) + ks * 128, sdesc_hi(1024), kIdPV,
+                       (u > 0 || ks > 0) ? 1u : 0u);
             }
           }
         }
@@ -247,12 +247,12 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t kbase = sbase + C::kKOff + st * C::kTileBytes;
         const uint32_t scol = tmem + (sb ? C::kColS1 : C::kColS0);
+        const uint32_t q_k = sdesc_lo(sbase + C::kQOff, 16), k_k = sdesc_lo(kbase, 16);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           // A = Q, B = K_j, both K-major: 16 head-dim elements = 32 B per step
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(scol, sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
+          const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          mma_ss_w(scol, q_k + o, k_k + o, sdesc_hi(1024), kIdQK, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF + sb));
         mma_commit(bar(C::kBKE + st));

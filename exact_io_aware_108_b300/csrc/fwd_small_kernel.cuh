@@ -189,13 +189,15 @@ __global__ void __launch_bounds__(256, 2)
       // S(t) = Q K(t)^T into the S columns
       auto issue_qk = [&](int t) {
         const uint32_t sb = opaque_u32(sbase);
-        const uint32_t kbase = sb + C::kKOff + (t % C::kKStages) * C::kTileBytes;
+        // descriptors as 32-bit words stepped by adds (sdesc_lo): few
+        // instructions per product for this thread
+        const uint32_t q_k = sdesc_lo(sb + C::kQOff, 16);
+        const uint32_t k_k = sdesc_lo(sb + C::kKOff + (t % C::kKStages) * C::kTileBytes, 16);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           // A = Q, B = K_j, both K-major: 16 channels = 32 B per step
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(sb + C::kQOff + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                 kIdQK, k > 0 ? 1u : 0u);
+          const uint32_t o = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+          mma_ss_w(tmem + C::kColS, q_k + o, k_k + o, sdesc_hi(1024), kIdQK, k > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBSF));
         mma_commit(bar(C::kBKE + t % C::kKStages));
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(256, 2)
         }
         const int vs = t % C::kVStages;
         if (!mbar_wait(bar(C::kBVF + vs), (t / C::kVStages) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t vbase = opaque_u32(sbase) + C::kVOff + vs * C::kTileBytes;
+        const uint32_t v_mn = sdesc_lo(opaque_u32(sbase) + C::kVOff + vs * C::kTileBytes, 16384);
         // O += P(t) V(t) in two halves of 64 keys
         for (int h = 0; h < 2; ++h) {
           if (!mbar_wait(bar(C::kBPF + h), ph, abort_flag)) { ok = false; break; }
@@ -236,8 +238,8 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
           for (int k = 4 * h; k < 4 * h + 4; ++k)
             // B = V_j, MN-major: 16 keys per step = 16 rows of 128 B
-            mma_ts(tmem + C::kColO, tmem + C::kColP + k * 8, sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdPV,
-                   (t > 0 || k > 0) ? 1u : 0u);
+            mma_ts_w(tmem + C::kColO, tmem + C::kColP + k * 8, v_mn + k * 128, sdesc_hi(1024), kIdPV,
+                     (t > 0 || k > 0) ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(bar(C::kBVE + vs));
