@@ -347,7 +347,25 @@ struct BwdCfg {
   // MMA order: S_{i+1} right after dV_i (d = 64) or after dQ_i (d = 128,
   // where the Q load of tile i+1 needs the longer window); both measured.
   static constexpr bool kSAfterDV = (D == 64);
+  // d = 128: the two dO stages and the dS^T buffer are three 32 KB buffers
+  // in a row whose roles rotate: dO of tile u goes to buffer u % 3 and dS^T
+  // of tile u to buffer (u + 2) % 3, the one that held dO of tile u - 1
+  // (its readers, dP and dV of tile u - 1, are done once dP of tile u is:
+  // a commit covers every earlier product). So writing dS^T never waits for
+  // the previous tile's dQ and dK products, which read the third buffer;
+  // a buffer goes dO(u) -> dS^T(u + 1) -> dO(u + 3), refilled once dK of
+  // tile u + 1 is done, which is the Q stage's release. (At d = 64 a dO tile
+  // is 16 KB and dS^T 32 KB, so d = 64 keeps one dS^T buffer.)
+  static constexpr bool kRotDS = (D == 128);
+  // byte offsets of the dO tile and of the dS^T buffer of running tile u
+  __device__ static __forceinline__ uint32_t do_off(int u) {
+    return kdOOff + (kRotDS ? static_cast<unsigned>(u) % 3u : static_cast<unsigned>(u) & 1u) * kTileBytes;
+  }
+  __device__ static __forceinline__ uint32_t ds_off(int u) {
+    return kRotDS ? kdOOff + (static_cast<unsigned>(u) + 2u) % 3u * kTileBytes : kdSOff;
+  }
   static_assert(kColDP + 128 <= kTmemCols && kColDQ + (kDqT ? 128 : D) <= kTmemCols, "TMEM budget");
+  static_assert(!kRotDS || (kTileBytes == 32768 && kdSOff == kdOOff + 2 * kTileBytes), "rotation layout");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // setmaxnreg split: launch with 128 registers x 512 threads; warpgroup 0
   // (producer, MMA issuer) gives registers to the three compute warpgroups.
@@ -517,8 +535,8 @@ __global__ void __launch_bounds__(512, 1)
           for (int kb = 0; kb < C::kKB; ++kb) {
             tma_load_3d_hint(sbase + C::kQOff + st * C::kTileBytes + kb * 16384, &tm_q, bar(C::kBQF + st),
                              kb * 64, qi * 128, qh, pol_q);
-            tma_load_3d_hint(sbase + C::kdOOff + st * C::kTileBytes + kb * 16384, &tm_do,
-                             bar(C::kBQF + st), kb * 64, qi * 128, qh, pol_q);
+            tma_load_3d_hint(sbase + C::do_off(U) + kb * 16384, &tm_do, bar(C::kBQF + st), kb * 64, qi * 128,
+                             qh, pol_q);
           }
           const long long r0 = qh * tile_rows + static_cast<long long>(qi) * 128;
           bulk_load(sbase + C::kLseOff + st * 512, a.lse_l2 + r0, 512, bar(C::kBQF + st));
@@ -619,7 +637,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = 0; u < it.n_iter; ++u, ++U) {
           const int st = U & 1;
           const uint32_t sb = opaque_u32(sbase);
-          const uint32_t do_k = sdesc_lo(sb + C::kdOOff, 16) + st * kStageStep;
+          const uint32_t do_k = sdesc_lo(sb + C::do_off(U), 16);
           // d = 128: the dP^T columns hold the previous dQ partial until read out
           if (C::kDqT && U > 0 && !mbar_wait(bar(C::kBDQE), (U - 1) & 1, abort_flag)) { ok = false; break; }
           // the first dP^T of an item needs its V (in fp16)
@@ -641,7 +659,7 @@ __global__ void __launch_bounds__(512, 1)
           for (int h = 0; ok && h < 2; ++h) {
             if (!mbar_wait(bar(C::kBPR + h), U & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t do_mn = sdesc_lo(opaque_u32(sbase) + C::kdOOff, 16384) + st * kStageStep;
+            const uint32_t do_mn = sdesc_lo(opaque_u32(sbase) + C::do_off(U), 16384);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               mma_ts_w(tmem + C::kColDV, tmem + C::kColS + 64 * h + 8 * ks, do_mn + (4 * h + ks) * 128, kHi,
@@ -663,7 +681,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           // dQ first, so its read-out overlaps the next S^T and the dK MMA
           const uint32_t sb2 = opaque_u32(sbase);
-          const uint32_t k_mn = sdesc_lo(sb2 + C::kKOff, 16384), ds_mn = sdesc_lo(sb2 + C::kdSOff, 16384);
+          const uint32_t k_mn = sdesc_lo(sb2 + C::kKOff, 16384), ds_mn = sdesc_lo(sb2 + C::ds_off(U), 16384);
           if constexpr (C::kDqT) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // dQ_i^T = K_j^T dS^T (both MN-major in smem)
@@ -683,7 +701,7 @@ __global__ void __launch_bounds__(512, 1)
             issue_s(st ^ 1);
           }
           const uint32_t sb3 = opaque_u32(sbase);
-          const uint32_t ds_k = sdesc_lo(sb3 + C::kdSOff, 16);
+          const uint32_t ds_k = sdesc_lo(sb3 + C::ds_off(U), 16);
           const uint32_t q_mn = sdesc_lo(sb3 + C::kQOff, 16384) + st * kStageStep;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dK_j += dS^T Q_i (dS^T K-major in smem)
@@ -730,7 +748,6 @@ __global__ void __launch_bounds__(512, 1)
     // half's 64 per-query LSE and D values, read as 8 float2 each.
     const int t4 = lane >> 2, c4 = lane & 3;
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    const uint32_t sDS = sbase + C::kdSOff + h * 16384;
     int U = 0, kl = 0;
     for (int k = 0;; ++k) {
       int w;
@@ -827,8 +844,10 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive(bar(C::kBPR + h));
           if (!mbar_wait_warp(bar(C::kBDPF), U & 1, abort_flag)) { ok = false; break; }
-          // the previous dQ/dK MMAs must be done reading dS before it is rewritten
-          if (U > 0 && !mbar_wait_warp(bar(C::kBDSF), (U - 1) & 1, abort_flag)) { ok = false; break; }
+          // d = 64: the previous dQ/dK MMAs must be done reading dS before it
+          // is rewritten (d = 128 writes the rotated buffer, see BwdCfg)
+          if (!C::kRotDS && U > 0 && !mbar_wait_warp(bar(C::kBDSF), (U - 1) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t sDS = sbase + C::ds_off(U) + h * 16384;
           tc_fence_after();
           uint32_t dv[2][32];
           tmem_ld_16x256b_x8(tq + C::kColDP + 64 * h, dv[0]);
