@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "21decd4ed126577cf66ce5f014c9b9dcfcf9cacade135309329d1ac733d9b428",
-    "bytes_per_launch": {"4096": 4 * (204235520 + 83662592), "8192": 4 * (248574464 + 116528896),
-                         "16384": 4 * (249746176 + 120524288)},
+    "source_sha256": "a98dadda499e3f19feba697808be2c1d3cfbe5b7c4034a1d1391cd1d2dd54326",
+    "bytes_per_launch": {"4096": 4 * (204184320 + 83495424), "8192": 4 * (249155328 + 115978240),
+                         "16384": 4 * (249308928 + 118543872)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
