@@ -289,22 +289,30 @@ __global__ void __launch_bounds__(256) bwd_cvt_kernel(const BwdArgs a, long long
 }
 
 // ----------------------------------------------------------------- dq convert
-template <bool BF16>
-__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdArgs a, long long n_vec4, int D) {
-  // n_vec4 = BH * N * D / 4 output groups of 4 elements; the accumulator
-  // holds dQ * 2^-e_s (e_s as the main kernel recorded it)
+// dQ accumulator (fp32, dQ * 2^-e_s as the main kernel recorded e_s) -> dQ
+// (16-bit). Eight channels per thread (two 16-byte loads, one 16-byte
+// store); heads run along grid.y and rows along grid.x, so the per-head
+// padding of the accumulator's rows needs no division.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdArgs a, int BH) {
+  constexpr int kLanes = D / 8;          // threads per row
+  constexpr int kRows = 256 / kLanes;    // rows per block step
   const long long tile_rows = static_cast<long long>(a.nqt) * 128;
   const float u_s = exp2i(static_cast<int>(a.stats[3]));
-  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_vec4;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long e = g * 4;
-    const long long row = e / D, c = e % D;
-    const long long bh = row / a.N, i = row % a.N;
-    const float4 v = *reinterpret_cast<const float4 *>(a.dq_acc + (bh * tile_rows + i) * D + c);
-    uint2 out;
-    out.x = pack2<BF16>(v.x * u_s, v.y * u_s);
-    out.y = pack2<BF16>(v.z * u_s, v.w * u_s);
-    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.dq) + e) = out;
+  const int sub = static_cast<int>(threadIdx.x) % kLanes, r0 = static_cast<int>(threadIdx.x) / kLanes;
+  for (int bh = static_cast<int>(blockIdx.y); bh < BH; bh += static_cast<int>(gridDim.y)) {
+    const float *acc = a.dq_acc + static_cast<size_t>(bh) * tile_rows * D + sub * 8;
+    uint16_t *out = static_cast<uint16_t *>(a.dq) + static_cast<size_t>(bh) * a.N * D + sub * 8;
+    for (int i = static_cast<int>(blockIdx.x) * kRows + r0; i < a.N; i += static_cast<int>(gridDim.x) * kRows) {
+      const float4 *src = reinterpret_cast<const float4 *>(acc + static_cast<size_t>(i) * D);
+      const float4 v0 = src[0], v1 = src[1];
+      uint4 o;
+      o.x = pack2<BF16>(v0.x * u_s, v0.y * u_s);
+      o.y = pack2<BF16>(v0.z * u_s, v0.w * u_s);
+      o.z = pack2<BF16>(v1.x * u_s, v1.y * u_s);
+      o.w = pack2<BF16>(v1.z * u_s, v1.w * u_s);
+      *reinterpret_cast<uint4 *>(out + static_cast<size_t>(i) * D) = o;
+    }
   }
 }
 

@@ -568,9 +568,13 @@ fa_status launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if (r != FA_OK) return r;
   }
   if (phases & kFinish) {
-    long long dq_blocks = (n_vec4 + 255) / 256;
-    if (dq_blocks > 148 * 16) dq_blocks = 148 * 16;
-    fa::bwd_dq_kernel<BF16><<<static_cast<int>(dq_blocks), 256, 0, st>>>(a, n_vec4, D);
+    // heads along y, rows along x: about 16 blocks of 256 threads per SM
+    const long long bh = n_vec4 * 4 / (static_cast<long long>(a.N) * D);
+    const int gy = static_cast<int>(std::min<long long>(bh, 65535));
+    constexpr int kRows = 256 / (D / 8);
+    const long long rows_x = (a.N + kRows - 1) / kRows;
+    const int gx = static_cast<int>(std::max<long long>(1, std::min<long long>(rows_x, (148ll * 16 + gy - 1) / gy)));
+    fa::bwd_dq_kernel<BF16, D><<<dim3(gx, gy), 256, 0, st>>>(a, static_cast<int>(bh));
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "bwd finish launch");
   }
