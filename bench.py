@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "a98dadda499e3f19feba697808be2c1d3cfbe5b7c4034a1d1391cd1d2dd54326",
-    "bytes_per_launch": {"4096": 4 * (204184320 + 83495424), "8192": 4 * (249155328 + 115978240),
-                         "16384": 4 * (249308928 + 118543872)},
+    "source_sha256": "060b0371c94c5f01064cee9a48373fae4637758ea3d96ae169c359c2b8e94f84",
+    "bytes_per_launch": {"4096": 4 * (204081920 + 83421184), "8192": 4 * (248869632 + 115957248),
+                         "16384": 4 * (250276608 + 120120064)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
