@@ -298,9 +298,9 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
 /*
  * Grouped-query backward (the gradients of fa_fwd_gqa): dq [B,H,N,d] per
  * query head; dk, dv [B,Hkv,N,d], each the sum over the H / Hkv query heads
- * that read that key/value head. One CTA per (batch, key/value head, key
- * tile) walks every query head of its group, so dK and dV are accumulated
- * on chip and stay deterministic. Other arguments as in fa_bwd; the
+ * that read that key/value head. Each work item (batch, key/value head,
+ * key tile) is walked by one CTA over every query head of its group, so dK
+ * and dV are accumulated on chip and stay deterministic. Other arguments as in fa_bwd; the
  * workspace is fa_bwd_workspace_size(B, H, N, d) (query rows).
  */
 fa_status fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
