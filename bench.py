@@ -48,7 +48,8 @@ TRAFFIC = {
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
                   "exact_io_aware_108_b300/csrc/ptx.cuh",
-                  "exact_io_aware_108_b300/csrc/schedule.cuh"]
+                  "exact_io_aware_108_b300/csrc/schedule.cuh",
+                  "exact_io_aware_108_b300/csrc/sdesc.cuh"]
 
 
 def kernel_sha():

@@ -4,6 +4,7 @@
 // Everything here is a thin wrapper over one documented PTX instruction, so
 // the kernels read as the sequence of hardware operations they issue.
 #pragma once
+#include "sdesc.cuh"
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -249,37 +250,6 @@ __device__ __forceinline__ void reg_fence_32(uint32_t (&r)[32]) {
   asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
-//   K-major operand (rows of 64 16-bit elements = 128 B, 8-row atoms of 1 KB):
-//     lbo unused (16), sbo = 1024 (next 8-row group); step K by 16 elements
-//     by adding 32 bytes to the start address.
-//   MN-major operand (rows = K index, 64 MN elements per 128-B row):
-//     lbo = byte distance between 64-element MN chunks, sbo = 1024 (next
-//     8 K-rows); step K by 16 by adding 2048 bytes.
-// Bits: [0,14) start>>4, [16,30) lbo>>4, [32,46) sbo>>4, [46,48) version 1,
-// [49,52) base offset 0 (atoms are 1 KB aligned), [61,64) layout 2 = SW128.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// The same descriptor as two 32-bit words, for issue loops that step the
-// start address: lo = start >> 4 | (LBO >> 4) << 16, hi = SBO >> 4 | the
-// version and swizzle bits. The descriptor of start + off (off a multiple of
-// 16) is {lo + off / 16, hi}: the start-address field is 14 bits wide and
-// shared-memory addresses stay below 2^18, so the add never carries into
-// the LBO field.
-__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
-  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
-}
-__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo) {
-  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-}
 // mma_ss / mma_ts with the descriptors as {lo, hi} words (hi constant).
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                                         uint32_t idesc, uint32_t accumulate) {
