@@ -389,10 +389,31 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     assert fa.fa_get_device_error(stream) == 0, "device error in the end-to-end timing"
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_k, dist, device)
+    # the copies alone (same bytes, same two copy streams, no compute): the
+    # floor the end-to-end step is held to by the host link
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    c0.record(stream)
+    h2d.wait_event(c0)
+    d2h.wait_event(c0)
+    for _ in range(e2e_k):
+        for p in probs:
+            with torch.cuda.stream(h2d):
+                p.copy_in(h2d)
+            with torch.cuda.stream(d2h):
+                p.copy_out(d2h)
+    for cs in (h2d, d2h):
+        ev = torch.cuda.Event()
+        ev.record(cs)
+        stream.wait_event(ev)
+    c1.record(stream)
+    barrier()
+    copy_ms = max_over_ranks(c0.elapsed_time(c1) / e2e_k, dist, device)
     e2e = {"value": round(whole_job_rate(flops_step, e2e_ms, world), 1), "unit": "TFLOP/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes() for p in probs),
            "d2h_bytes_per_step": sum(p.d2h_bytes() for p in probs),
            "ms_per_step": round(e2e_ms, 3),
+           "copies_alone_ms_per_step": round(copy_ms, 3),
            "overlap": "h2d, compute and d2h on three streams; one sweep point's copies "
                       "overlap the others' compute"}
 
