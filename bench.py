@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "060b0371c94c5f01064cee9a48373fae4637758ea3d96ae169c359c2b8e94f84",
-    "bytes_per_launch": {"4096": 4 * (204081920 + 83421184), "8192": 4 * (248869632 + 115957248),
-                         "16384": 4 * (250276608 + 120120064)},
+    "source_sha256": "d9ad9adeabc0208b3286325ba8d22b97255e280b1c9107f4e904a0fccdd939a9",
+    "bytes_per_launch": {"4096": 4 * (204316160 + 83747584), "8192": 4 * (249880576 + 116498176),
+                         "16384": 4 * (251365632 + 120796928)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
