@@ -763,6 +763,9 @@ __global__ void __launch_bounds__(512, 1)
       const BwdItem it = bwd_item<CAUSAL, SPARSE>(a, w);
       const int kt = it.kt, kvl = it.kvl;
       bool ok = !*abort_flag, have = false;
+      // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO); read
+      // again per item rather than kept in a register through the tile loop
+      float f_out = 1.f;
       if (ok && it.n_iter > 0) {
         // ---- bf16 inputs: K_j, then V_j -> fp16 in place. The first S^T
         // needs only K; the first dP^T waits for V.
@@ -904,45 +907,83 @@ __global__ void __launch_bounds__(512, 1)
           mbar_arrive(bar(C::kBDSR));
           advance(it, g, qi);
         }
+        // the output factor's global load overlaps the wait
+        f_out = exp2i(h == 0 ? ds_exponent(a.stats, a.scale, D) : (BF16 ? do_exponent(a.stats) : 0));
         have = ok && mbar_wait_warp(bar(C::kBFIN), kl & 1, abort_flag);
         if (have) tc_fence_after();
         ++kl;
       }
-      // ---- dK (warpgroup 1) or dV (warpgroup 2), 32 channels at a time out
-      // of TMEM (zeros for an item without work or after a stop); the next
+      // ---- dK (warpgroup 1) or dV (warpgroup 2) out of TMEM; the next
       // item's first dV product waits until both are read
-      const int key = kt * 128 + r;
-      uint16_t *dst = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
-                      (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(key)) * D;
-      // dK carries 2^-e_s (from dS), dV carries 2^-e_do (from dO); read again
-      // here rather than kept in a register through the tile loop
-      const float f_out = exp2i(h == 0 ? ds_exponent(a.stats, a.scale, D) : (BF16 ? do_exponent(a.stats) : 0));
-#pragma unroll 1
-      for (int j = 0; j < D / 32; ++j) {
-        uint32_t v[32];
-        if (have) {
-          tmem_ld_32x32b_x32(tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV) + 32 * j, v);
-          tmem_wait_ld();
-          reg_fence_32(v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (key < a.N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * j);
-          float x[32];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            fmul2(x[i], x[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), f_out, f_out);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack2<BF16>(x[8 * q], x[8 * q + 1]), pack2<BF16>(x[8 * q + 2], x[8 * q + 3]),
-                               pack2<BF16>(x[8 * q + 4], x[8 * q + 5]), pack2<BF16>(x[8 * q + 6], x[8 * q + 7]));
-        }
-      }
+      const uint32_t acc_col = tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV);
+      // after a stop the warps of a warpgroup may disagree (each left its
+      // waits on its own); the boxes below need all four, so they go on
+      // only if every warp has the item's results
+      have = named_bar_and(2 + h, 128, have);
       if (have) {
-        tc_fence_before();
-        mbar_arrive(bar(C::kBACC));
+        // 64 channels at a time: each thread puts its key row's channels into
+        // a 16 KB staging box (128-byte rows, 16-byte chunks swizzled by the
+        // row, so neither pass has bank conflicts), then the warpgroup writes
+        // the box out eight threads per 128-byte row piece: four whole lines
+        // per warp instruction. Rows past N are not written. The box is this
+        // half's part of the buffer the next dS^T goes to: the products that
+        // read it last (dS^T of the item's last tile at d = 64, dO of that
+        // tile at d = 128) are done (kBFIN), and the next writer is this
+        // warpgroup, after the last barrier below. Stores straight from
+        // registers (a 16-byte piece of each of 32 rows per warp instruction)
+        // kept the memory pipeline busy for longer than a tile, and TMA
+        // stores of the box took almost as long to release it; both held up
+        // the next item's start.
+        const uint32_t stage = sbase + C::ds_off(U) + h * 16384;
+#pragma unroll 1
+        for (int c64 = 0; c64 < D; c64 += 64) {
+          if (c64 > 0) named_bar_sync(2 + h, 128);  // the previous box has been read
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(acc_col + c64 + c0, v);
+            tmem_wait_ld();
+            reg_fence_32(v);
+            uint32_t pw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              fmul2(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), f_out, f_out);
+              pw[i] = pack2<BF16>(x0, x1);
+            }
+            // channels c0 .. c0 + 31 of the box are 16-byte chunks c0 / 8 .. +3 of row r
+            const uint32_t rbase = stage + r * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(rbase + (static_cast<uint32_t>((c0 / 8 + q) ^ (r & 7)) << 4), pw[4 * q], pw[4 * q + 1],
+                           pw[4 * q + 2], pw[4 * q + 3]);
+          }
+          if (c64 + 64 == D) {  // every accumulator column has been read
+            tc_fence_before();
+            mbar_arrive(bar(C::kBACC));
+          }
+          named_bar_sync(2 + h, 128);
+          const int rows = min(128, a.N - kt * 128);
+          const int cc = r & 7;  // 16-byte chunk of the write-out pass
+          uint16_t *out = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
+                          (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(kt) * 128) * D + c64 + cc * 8;
+#pragma unroll 4
+          for (int i = 0; i < 8; ++i) {
+            const int row = 16 * i + (r >> 3);
+            const uint4 w = ld_shared_v4(stage + row * 128 + (static_cast<uint32_t>(cc ^ (row & 7)) << 4));
+            if (row < rows) *reinterpret_cast<uint4 *>(out + static_cast<size_t>(row) * D) = w;
+          }
+        }
+        // the box has been read before this warpgroup writes dS^T into it
+        named_bar_sync(2 + h, 128);
+      } else {
+        // zeros (an item without work, or after a stop), row by row
+        const int key = kt * 128 + r;
+        if (key < a.N) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
+                                                (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(key)) * D);
+          for (int q = 0; q < D / 8; ++q) d4[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     } else {

@@ -88,6 +88,18 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                "r"(x), "r"(y), "r"(z), "r"(src)
                : "memory");
 }
+// 16-byte shared-memory store (four 32-bit words).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+               : "memory");
+}
+// 16-byte shared-memory load.
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
 // Closes the bulk group of the stores issued so far by this thread.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has read its
@@ -119,6 +131,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // Named CTA barrier `id` over `count` threads (count a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named CTA barrier that also ANDs a predicate over its `count` threads:
+// every thread gets true only if all of them passed true.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0u;
 }
 
 // ------------------------------------------------------------------ tcgen05
