@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "d9ad9adeabc0208b3286325ba8d22b97255e280b1c9107f4e904a0fccdd939a9",
-    "bytes_per_launch": {"4096": 4 * (204316160 + 83747584), "8192": 4 * (249880576 + 116498176),
-                         "16384": 4 * (251365632 + 120796928)},
+    "source_sha256": "86e86558a2c425c3b8ad952af1050a5f1d58e95044c823322022317f89cfab5e",
+    "bytes_per_launch": {"4096": 4 * (205092352 + 85838336), "8192": 4 * (255592704 + 119843840),
+                         "16384": 4 * (256977920 + 123765504)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
