@@ -916,28 +916,23 @@ __global__ void __launch_bounds__(512, 1)
       // ---- dK (warpgroup 1) or dV (warpgroup 2) out of TMEM; the next
       // item's first dV product waits until both are read
       const uint32_t acc_col = tmem + lane_addr + (h == 0 ? C::kColDK : C::kColDV);
-      // after a stop the warps of a warpgroup may disagree (each left its
-      // waits on its own); the boxes below need all four, so they go on
-      // only if every warp has the item's results
-      have = named_bar_and(2 + h, 128, have);
       if (have) {
         // 64 channels at a time: each thread puts its key row's channels into
-        // a 16 KB staging box (128-byte rows, 16-byte chunks swizzled by the
-        // row, so neither pass has bank conflicts), then the warpgroup writes
-        // the box out eight threads per 128-byte row piece: four whole lines
-        // per warp instruction. Rows past N are not written. The box is this
-        // half's part of the buffer the next dS^T goes to: the products that
-        // read it last (dS^T of the item's last tile at d = 64, dO of that
-        // tile at d = 128) are done (kBFIN), and the next writer is this
-        // warpgroup, after the last barrier below. Stores straight from
-        // registers (a 16-byte piece of each of 32 rows per warp instruction)
-        // kept the memory pipeline busy for longer than a tile, and TMA
-        // stores of the box took almost as long to release it; both held up
-        // the next item's start.
-        const uint32_t stage = sbase + C::ds_off(U) + h * 16384;
+        // this warp's 4 KB slice of a staging box (its 32 rows of 128 bytes,
+        // 16-byte chunks swizzled by the row, so neither pass has bank
+        // conflicts), then the warp writes its rows out eight threads per
+        // 128-byte row piece: four whole lines per warp instruction. Rows
+        // past N are not written. The slice lies in this half's part of the
+        // buffer the next dS^T goes to, in the rows this warp writes there:
+        // the products that read it last (dS^T of the item's last tile at
+        // d = 64, dO of that tile at d = 128) are done (kBFIN), and no other
+        // warp touches it, so the warps need not wait for one another.
+        // Stores straight from registers (a 16-byte piece of each of 32 rows
+        // per warp instruction) kept the memory pipeline busy for longer
+        // than a tile and held up the next item's start.
+        const uint32_t slice = sbase + C::ds_off(U) + h * 16384 + (warp & 3) * 4096;
 #pragma unroll 1
         for (int c64 = 0; c64 < D; c64 += 64) {
-          if (c64 > 0) named_bar_sync(2 + h, 128);  // the previous box has been read
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t v[32];
@@ -951,31 +946,30 @@ __global__ void __launch_bounds__(512, 1)
               fmul2(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), f_out, f_out);
               pw[i] = pack2<BF16>(x0, x1);
             }
-            // channels c0 .. c0 + 31 of the box are 16-byte chunks c0 / 8 .. +3 of row r
-            const uint32_t rbase = stage + r * 128;
+            // channels c0 .. c0 + 31 are 16-byte chunks c0 / 8 .. +3 of the row
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_shared_v4(rbase + (static_cast<uint32_t>((c0 / 8 + q) ^ (r & 7)) << 4), pw[4 * q], pw[4 * q + 1],
-                           pw[4 * q + 2], pw[4 * q + 3]);
+              st_shared_v4(slice + lane * 128 + (static_cast<uint32_t>((c0 / 8 + q) ^ (lane & 7)) << 4), pw[4 * q],
+                           pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
           }
           if (c64 + 64 == D) {  // every accumulator column has been read
             tc_fence_before();
             mbar_arrive(bar(C::kBACC));
           }
-          named_bar_sync(2 + h, 128);
-          const int rows = min(128, a.N - kt * 128);
-          const int cc = r & 7;  // 16-byte chunk of the write-out pass
+          __syncwarp();
+          const int rows = min(32, a.N - kt * 128 - 32 * (warp & 3));  // this warp's rows inside N
+          const int cc = lane & 7;  // 16-byte chunk of the write-out pass
           uint16_t *out = static_cast<uint16_t *>(h == 0 ? a.dk : a.dv) +
-                          (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(kt) * 128) * D + c64 + cc * 8;
+                          (static_cast<size_t>(it.bkv) * a.N + static_cast<size_t>(kt) * 128 + 32 * (warp & 3)) * D +
+                          c64 + cc * 8;
 #pragma unroll 4
           for (int i = 0; i < 8; ++i) {
-            const int row = 16 * i + (r >> 3);
-            const uint4 w = ld_shared_v4(stage + row * 128 + (static_cast<uint32_t>(cc ^ (row & 7)) << 4));
+            const int row = 4 * i + (lane >> 3);
+            const uint4 w = ld_shared_v4(slice + row * 128 + (static_cast<uint32_t>(cc ^ (row & 7)) << 4));
             if (row < rows) *reinterpret_cast<uint4 *>(out + static_cast<size_t>(row) * D) = w;
           }
+          __syncwarp();  // the slice has been read before it is written again
         }
-        // the box has been read before this warpgroup writes dS^T into it
-        named_bar_sync(2 + h, 128);
       } else {
         // zeros (an item without work, or after a stop), row by row
         const int key = kt * 128 + r;

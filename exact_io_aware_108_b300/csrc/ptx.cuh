@@ -133,19 +133,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Named CTA barrier that also ANDs a predicate over its `count` threads:
-// every thread gets true only if all of them passed true.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0u;
-}
-
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation: executed by one full warp; the TMEM address is written
 // to shared memory at dst.
