@@ -41,9 +41,9 @@ WORKLOAD_NAME = ("long-context causal attention sweep N in {4096, 8192, 16384}, 
 # sources hashed in "source_sha256". Measured on B/4 of each sweep point (one
 # launch) and scaled by 4: the DRAM bytes grow with the number of heads.
 TRAFFIC = {
-    "source_sha256": "86e86558a2c425c3b8ad952af1050a5f1d58e95044c823322022317f89cfab5e",
-    "bytes_per_launch": {"4096": 4 * (205092352 + 85838336), "8192": 4 * (255592704 + 119843840),
-                         "16384": 4 * (256977920 + 123765504)},
+    "source_sha256": "7c0999cac1f02e345deb6c00d195d43119fd12cc38f94597115772a1b78d15fb",
+    "bytes_per_launch": {"4096": 4 * (205226496 + 85993216), "8192": 4 * (256429824 + 119474432),
+                         "16384": 4 * (257691904 + 123221504)},
 }
 KERNEL_SOURCES = ["exact_io_aware_108_b300/csrc/bwd_kernel.cuh",
                   "exact_io_aware_108_b300/csrc/common.cuh",
