@@ -14,6 +14,7 @@ the timing is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -81,15 +82,23 @@ REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_powe
 
 
 class ClockSampler:
-    def __init__(self, gpu_id):
+    """nvidia-smi samples of the SM clock and the throttle reasons every 50 ms;
+    the summary keeps the samples whose timestamps fall between mark_start()
+    and mark_end() (the timed region), so the idle GPU before and after it
+    does not enter the median."""
+
+    def __init__(self, gpu_id, interval_ms=50):
         self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
         self.proc = None
-        self.path = None
+        self.lines = []
+        self.t_start = self.t_end = None
 
     def __enter__(self):
-        q = ("clocks.sm,clocks.max.sm,power.draw," +
+        q = ("timestamp,clocks.sm,clocks.max.sm,power.draw," +
              ",".join("clocks_event_reasons." + r for r in REASONS))
-        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms",
+               str(self.interval_ms)]
         if self.gpu_id is not None:
             cmd += ["-i", str(self.gpu_id)]
         try:
@@ -100,32 +109,50 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
     def __exit__(self, *exc):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.1)
             self.proc.terminate()
             out, _ = self.proc.communicate(timeout=10)
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
+    @staticmethod
+    def parse(line):
+        """(unix time, sm MHz, max sm MHz, set of active reasons) or None."""
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 4 + len(REASONS):
+            return None
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, mx = float(parts[1]), float(parts[2])
+        except ValueError:
+            return None
+        reasons = {r for r, v in zip(REASONS, parts[4:]) if v.lower() == "active"}
+        return ts, sm, mx, reasons
+
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        for ln in getattr(self, "lines", []):
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 3 + len(REASONS):
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for r, v in zip(REASONS, parts[3:]):
-                if v.lower() == "active":
-                    reasons.add(r)
-        if not sm:
+        samples = [x for x in (self.parse(ln) for ln in self.lines) if x is not None]
+        inside = samples
+        if self.t_start is not None and self.t_end is not None:
+            inside = [x for x in samples if self.t_start <= x[0] <= self.t_end]
+        in_window = bool(inside)
+        if not inside:  # a region shorter than the sampling interval
+            inside = samples
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set()
+        for x in inside:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if in_window else "whole sampling period"}
 
 
 # ------------------------------------------------------------------ ranks
@@ -260,6 +287,7 @@ def run_ours(args, rank, world, local_rank):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(gpu_uuid) as clocks:
+        clocks.mark_start()
         with torch.cuda.stream(stream):
             t0.record(stream)
             for s in range(K):
@@ -267,6 +295,7 @@ def run_ours(args, rank, world, local_rank):
                     p.step(stream, main_events=main_ev[s][i], fwd_events=fwd_ev[s][i])
             t1.record(stream)
         barrier()
+        clocks.mark_end()
     ms_total = t0.elapsed_time(t1)
     assert fa.fa_get_device_error(stream) == 0, "device error in the timed region"
     ms_max = max_over_ranks(ms_total, dist, device)
